@@ -1,0 +1,415 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests retypes an oracle formula: each compares the oracle with
+a worked example printed on the pages, a brute force on tiny inputs, a
+closed form, finite differences of an independently written forward pass, or
+an identity the LRMoE paper states. The mutation tests at the end plant
+plausible mistakes in the oracle and check that a pin catches each one.
+"""
+
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import lrm_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    rows = {}
+    groups = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "group":
+                groups[int(vals[0])] = vals[1:]
+            else:
+                rows[key] = vals
+    return rows, groups
+
+
+def _rand_topk(rng, T, K, E):
+    """Distinct experts per token, uniform."""
+    return np.stack([rng.choice(E, size=K, replace=False) for _ in range(T)])
+
+
+def _tiny_layer(rng, T=12, D=6, H=5, E=4, K=2, consistent=True):
+    """A tiny fp64 layer with saved state computed by an explicit forward."""
+    x = rng.standard_normal((T, D))
+    g = rng.standard_normal((T, D)) * np.exp(0.5 * rng.standard_normal(T))[:, None]
+    wg = rng.standard_normal((E, D, H)) / math.sqrt(D)
+    wu = rng.standard_normal((E, D, H)) / math.sqrt(D)
+    wd = rng.standard_normal((E, H, D)) / math.sqrt(D)
+    topk = _rand_topk(rng, T, K, E)
+    alpha = rng.uniform(0.05, 0.5, size=(T, K))
+    N = T * K
+    ab = np.zeros((N, 2 * H))
+    phi = np.zeros((N, H))
+    for t in range(T):
+        for k in range(K):
+            e = topk[t, k]
+            a = x[t] @ wg[e]
+            b = x[t] @ wu[e]
+            ab[t * K + k] = np.concatenate([a, b])
+            phi[t * K + k] = a / (1.0 + np.exp(-a)) * b
+    if not consistent:
+        phi = rng.standard_normal((N, H))
+    return dict(x=x, g=g, wg=wg, wu=wu, wd=wd, topk=topk, alpha=alpha,
+                ab=ab, phi=phi, T=T, D=D, H=H, E=E, K=K)
+
+
+# ---------------------------------------------------------------------------
+# dispatch permutation
+# ---------------------------------------------------------------------------
+def test_reindex_worked_example():
+    rows, groups = _read_golden("llep_reindex_example.txt")
+    tokens = rows["tokens"]
+    experts = np.array([int(v) for v in rows["experts"]])[:, None]
+    perm, inv, counts, off = oracle.dispatch_permute(experts, E=8)
+    assert [tokens[p] for p in perm] == rows["reindexed"]
+    for e, members in groups.items():
+        seg = perm[off[e]:off[e + 1]]
+        assert [tokens[p] for p in seg] == members
+    assert counts.sum() == 4 and counts[1] == 1 and counts[2] == 2 and counts[6] == 1
+
+
+@pytest.mark.parametrize("T,K,E,seed", [(1, 1, 1, 0), (7, 2, 5, 1), (50, 4, 16, 2),
+                                        (33, 8, 64, 3)])
+def test_dispatch_matches_python_stable_sort(T, K, E, seed):
+    rng = np.random.default_rng(seed)
+    topk = _rand_topk(rng, T, K, E)
+    flat = topk.reshape(-1)
+    perm, inv, counts, off = oracle.dispatch_permute(topk, E)
+    brute = sorted(range(T * K), key=lambda p: flat[p])  # Python's sort is stable
+    assert list(perm) == brute
+    assert np.array_equal(inv[perm], np.arange(T * K))
+    for e in range(E):
+        assert counts[e] == sum(1 for v in flat if v == e)
+        assert off[e + 1] - off[e] == counts[e]
+    assert off[0] == 0 and off[-1] == T * K
+
+
+def test_dispatch_rejects_bad_expert_id():
+    with pytest.raises(ValueError):
+        oracle.dispatch_permute(np.array([[0], [4]]), E=4)
+
+
+# ---------------------------------------------------------------------------
+# quota rule
+# ---------------------------------------------------------------------------
+def test_quota_exact_ceiling_against_fractions():
+    counts = np.arange(0, 40000)
+    for num, den in [(1, 4), (1, 2), (3, 5), (3, 4), (1, 1), (0, 1)]:
+        q = oracle.quota_from_rate(counts, num, den)
+        want = [math.ceil(Fraction(num, den) * int(n)) for n in counts]
+        assert list(q) == want
+    # the floating-point ceiling goes wrong for some n, the exact one does not
+    bad = [n for n in range(1, 40000)
+           if math.ceil(np.float32(0.6) * np.float32(n)) != math.ceil(Fraction(3, 5) * n)]
+    assert len(bad) > 0
+
+
+def test_quota_cap():
+    q = oracle.quota_from_rate(np.array([0, 1, 2559, 2560, 2561, 32768]), 1, 2, cap=1280)
+    assert list(q) == [0, 1, 1280, 1280, 1280, 1280]
+    assert list(oracle.quota_from_rate(np.array([3, 9]), 1, 1)) == [3, 9]
+
+
+# ---------------------------------------------------------------------------
+# LRM score
+# ---------------------------------------------------------------------------
+def test_score_equals_bruteforce_frobenius_norm():
+    rng = np.random.default_rng(5)
+    L = _tiny_layer(rng, T=9, D=7, H=5, E=5, K=3, consistent=False)
+    K = L["K"]
+    flat = L["topk"].reshape(-1)
+    perm, inv, counts, off = oracle.dispatch_permute(L["topk"], L["E"])
+    brute_perm = sorted(range(flat.size), key=lambda p: flat[p])
+    phi_disp = L["phi"][brute_perm]
+    R = oracle.score(L["g"], phi_disp, L["alpha"], perm, K)
+    for pos, p in enumerate(brute_perm):
+        t, k = divmod(p, K)
+        G = np.outer(L["alpha"][t, k] * L["g"][t], phi_disp[pos])  # (alpha g) phi^T
+        assert R[pos] == pytest.approx(np.sum(G * G), rel=1e-12)
+
+
+def test_score_closed_form_constant_inputs():
+    T, D, H, K = 3, 4, 6, 2
+    topk = np.array([[0, 1], [1, 2], [2, 0]])
+    alpha = np.array([[0.5, 0.25], [0.125, 1.0], [2.0, 0.75]])
+    perm, *_ = oracle.dispatch_permute(topk, 3)
+    R = oracle.score(np.ones((T, D)), np.full((T * K, H), 2.0), alpha, perm, K)
+    for pos, p in enumerate(perm):
+        assert R[pos] == alpha.reshape(-1)[p] ** 2 * D * (4.0 * H)
+
+
+# ---------------------------------------------------------------------------
+# selection
+# ---------------------------------------------------------------------------
+def _select_case(rng, n_per_expert, integer_scores):
+    E = len(n_per_expert)
+    experts = np.concatenate([[e] * n for e, n in enumerate(n_per_expert)]).astype(np.int64)
+    rng.shuffle(experts)
+    perm, inv, counts, off = oracle.dispatch_permute(experts[:, None], E)
+    N = experts.size
+    R = (rng.integers(0, 4, size=N).astype(float) if integer_scores
+         else rng.random(N))
+    return perm, off, R
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_select_is_optimal_and_unique_under_tie_rule(seed):
+    rng = np.random.default_rng(seed)
+    sizes = [int(v) for v in rng.integers(0, 10, size=5)]
+    perm, off, R = _select_case(rng, sizes, integer_scores=(seed % 2 == 0))
+    quota = np.array([int(rng.integers(0, n + 1)) for n in sizes])
+    keep, sel_off, sel_pos = oracle.select_quota(R, off, quota, perm)
+    assert list(np.diff(sel_off)) == list(quota)
+    for e, n in enumerate(sizes):
+        seg = list(range(off[e], off[e + 1]))
+        q = quota[e]
+        chosen = [pos for pos in seg if keep[pos]]
+        assert chosen == list(sel_pos[sel_off[e]:sel_off[e + 1]])
+        best = max((sum(R[i] for i in c) for c in itertools.combinations(seg, q)),
+                   default=0.0)
+        assert sum(R[i] for i in chosen) == pytest.approx(best)  # Prop. 7.1
+
+        def tie_ok(c):
+            dropped = [j for j in seg if j not in c]
+            return all(R[i] > R[j] or (R[i] == R[j] and perm[i] < perm[j])
+                       for i in c for j in dropped)
+        valid = [list(c) for c in itertools.combinations(seg, q) if tie_ok(c)]
+        assert valid == [chosen]
+
+
+def test_compaction_worked_example_fig4():
+    rows, _ = _read_golden("lrmoe_fig4_compaction.txt")
+    loads = [int(v) for v in rows["loads"]]
+    quotas = np.array([int(v) for v in rows["quotas"]])
+    rng = np.random.default_rng(0)
+    perm, off, R = _select_case(rng, loads, integer_scores=False)
+    assert list(np.diff(off)) == loads
+    keep, sel_off, sel_pos = oracle.select_quota(R, off, quotas, perm)
+    assert list(np.diff(sel_off)) == [int(v) for v in rows["groups"]]
+    assert sel_pos.size == sum(int(v) for v in rows["groups"])
+
+
+def test_select_rejects_oversize_quota():
+    perm, off, R = _select_case(np.random.default_rng(1), [2, 3], False)
+    with pytest.raises(ValueError):
+        oracle.select_quota(R, off, np.array([3, 1]), perm)
+
+
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+def _forward_loss(x, wg, wu, wd, topk, alpha, g):
+    """Independent scalar L = sum_t g_t . sum_k alpha_tk FFN_e(x_t), fp64."""
+    T, K = topk.shape
+    L = 0.0
+    for t in range(T):
+        for k in range(K):
+            e = topk[t, k]
+            a = x[t] @ wg[e]
+            b = x[t] @ wu[e]
+            y = (a / (1.0 + np.exp(-a)) * b) @ wd[e]
+            L += alpha[t, k] * (g[t] @ y)
+    return L
+
+
+def _full_backward(L, num=1, den=1, quota=None):
+    return oracle.recalibrated_backward(
+        L["topk"], L["alpha"], L["x"], L["g"], L["ab"], L["phi"],
+        L["wg"], L["wu"], L["wd"], E=L["E"], num=num, den=den, quota=quota)
+
+
+def test_backward_matches_finite_differences_at_full_retention():
+    rng = np.random.default_rng(11)
+    L = _tiny_layer(rng, T=6, D=5, H=4, E=3, K=2)
+    out = _full_backward(L)
+    assert out["keep"].all()
+    h = 1e-6
+    args = dict(x=L["x"], wg=L["wg"], wu=L["wu"], wd=L["wd"])
+    grads = {"x": out["dx"], "wg": out["dw_gate"], "wu": out["dw_up"], "wd": out["dw_down"]}
+    for name, G in grads.items():
+        scale = np.abs(G).max()
+        for idx in itertools.islice(np.ndindex(G.shape), 0, None, 3):
+            plus = {k: v.copy() for k, v in args.items()}
+            minus = {k: v.copy() for k, v in args.items()}
+            plus[name][idx] += h
+            minus[name][idx] -= h
+            fd = (_forward_loss(**plus, topk=L["topk"], alpha=L["alpha"], g=L["g"]) -
+                  _forward_loss(**minus, topk=L["topk"], alpha=L["alpha"], g=L["g"])) / (2 * h)
+            assert abs(fd - G[idx]) <= 1e-6 * scale, (name, idx, fd, G[idx])
+
+
+@pytest.mark.parametrize("num,den", [(1, 2), (1, 4), (3, 5)])
+def test_compacted_equals_zero_masked_dense(num, den):
+    rng = np.random.default_rng(num * 10 + den)
+    L = _tiny_layer(rng, T=20, D=6, H=5, E=4, K=2)
+    out = _full_backward(L, num, den)
+    dWg, dWu, dWd, dx = oracle.expert_bwd_masked_dense(
+        out["keep"], out["off"], out["perm"], L["alpha"], L["x"], L["g"],
+        out["ab"], out["phi"], L["wg"], L["wu"], L["wd"], L["K"])
+    for a, b in [(out["dw_gate"], dWg), (out["dw_up"], dWu), (out["dw_down"], dWd),
+                 (out["dx"], dx)]:
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+    assert out["keep"].sum() < L["T"] * L["K"]
+
+
+def test_full_retention_is_identity_compaction_and_unpruned_backward():
+    rng = np.random.default_rng(3)
+    L = _tiny_layer(rng, T=10, D=4, H=3, E=5, K=2)
+    out = _full_backward(L, 1, 1)
+    N = L["T"] * L["K"]
+    assert np.array_equal(out["sel_pos"], np.arange(N))
+    assert np.array_equal(out["row_of_pos"], np.arange(N))
+    assert np.array_equal(out["ab_c"], out["ab"])
+    assert np.array_equal(out["phi_c"], out["phi"])
+    dWg, dWu, dWd, dx = oracle.expert_bwd_masked_dense(
+        np.ones(N), out["off"], out["perm"], L["alpha"], L["x"], L["g"],
+        out["ab"], out["phi"], L["wg"], L["wu"], L["wd"], L["K"])
+    np.testing.assert_allclose(out["dw_down"], dWd, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(out["dx"], dx, rtol=1e-12, atol=1e-14)
+
+
+def _dropped_contributions(L, out_full, out_part, e):
+    """G_u = phi_u^T delta_u (row convention) for the pairs of e dropped at rho."""
+    K = L["K"]
+    lo, hi = out_full["off"][e], out_full["off"][e + 1]
+    Gs, Rs = [], []
+    for pos in range(lo, hi):
+        if out_part["keep"][pos]:
+            continue
+        p = out_full["perm"][pos]
+        t, k = divmod(p, K)
+        Gs.append(np.outer(out_full["phi"][pos], L["alpha"][t, k] * L["g"][t]))
+        Rs.append(out_part["score"][pos])
+    return Gs, Rs
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_aggregate_error_relation_and_bound_eq19_20(seed):
+    rng = np.random.default_rng(100 + seed)
+    L = _tiny_layer(rng, T=24, D=6, H=5, E=3, K=2)
+    full = _full_backward(L, 1, 1)
+    part = _full_backward(L, 1, 2)
+    for e in range(L["E"]):
+        delta = full["dw_down"][e] - part["dw_down"][e]
+        Gs, Rs = _dropped_contributions(L, full, part, e)
+        d = len(Gs)
+        lhs = np.sum(delta * delta)
+        cross = sum(np.sum(Gs[u] * Gs[v]) for u in range(d) for v in range(u + 1, d))
+        assert lhs == pytest.approx(sum(Rs) + 2 * cross, rel=1e-9, abs=1e-12)  # Eq. 19
+        assert lhs <= sum(math.sqrt(r) for r in Rs) ** 2 * (1 + 1e-12) + 1e-15  # Eq. 20
+        assert sum(math.sqrt(r) for r in Rs) ** 2 <= d * sum(Rs) * (1 + 1e-12) + 1e-15
+
+
+def test_orthogonal_dropped_contributions_give_additive_error():
+    # one-hot saved inputs make every G_u of an expert Frobenius-orthogonal
+    rng = np.random.default_rng(7)
+    T, K, E, H, D = 8, 1, 1, 8, 3
+    L = _tiny_layer(rng, T=T, D=D, H=H, E=E, K=K)
+    L["phi"] = np.eye(T * K, H) * rng.uniform(0.5, 2.0, size=(T * K, 1))
+    full = _full_backward(L, 1, 1)
+    part = _full_backward(L, 1, 2)
+    delta = full["dw_down"][0] - part["dw_down"][0]
+    Gs, Rs = _dropped_contributions(L, full, part, 0)
+    assert len(Rs) == T // 2
+    assert np.sum(delta * delta) == pytest.approx(sum(Rs), rel=1e-12)
+
+
+def test_swiglu_grad_special_cases_and_derivative():
+    dphi = np.array([1.0, -2.0, 0.5])
+    b = np.array([3.0, 1.5, -1.0])
+    da, db = oracle.swiglu_grad(dphi, np.zeros(3), b)
+    assert np.allclose(da, dphi * b * 0.5) and np.allclose(db, 0.0)
+    da, db = oracle.swiglu_grad(dphi, np.full(3, 40.0), b)   # sigmoid -> 1
+    assert np.allclose(da, dphi * b) and np.allclose(db, dphi * 40.0)
+    rng = np.random.default_rng(0)
+    a = rng.standard_normal(5)
+    b = rng.standard_normal(5)
+    f = lambda a_, b_: a_ / (1 + np.exp(-a_)) * b_
+    h = 1e-6
+    da, db = oracle.swiglu_grad(np.ones(5), a, b)
+    assert np.allclose(da, (f(a + h, b) - f(a - h, b)) / (2 * h), atol=1e-8)
+    assert np.allclose(db, (f(a, b + h) - f(a, b - h)) / (2 * h), atol=1e-8)
+
+
+def test_sampled_rows_match_full_backward():
+    rng = np.random.default_rng(9)
+    L = _tiny_layer(rng, T=16, D=5, H=4, E=3, K=2)
+    out = _full_backward(L, 3, 5)
+    rows = np.arange(0, out["sel_pos"].size, 3)
+    dab, dxc = oracle.expert_bwd_rows(rows, out["sel_off"], L["wg"], L["wu"], L["wd"],
+                                      out["dy_c"], out["ab_c"])
+    np.testing.assert_allclose(dab, out["dab_c"][rows], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dxc, out["dx_c"][rows], rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must be caught by one of the pins above
+# ---------------------------------------------------------------------------
+def _wrong_swiglu_sign(dphi, a, b):
+    dphi, a, b = map(np.asarray, (dphi, a, b))
+    s = 1.0 / (1.0 + np.exp(-a))
+    return dphi * b * s * (1.0 - a * (1.0 - s)), dphi * a * s
+
+
+_ORIG_SCORE = orc.score
+_ORIG_DISPATCH = orc.dispatch_permute
+
+
+def _score_without_alpha(g, phi, alpha, perm, K):
+    return _ORIG_SCORE(g, phi, np.ones_like(np.asarray(alpha)), perm, K)
+
+
+_ORIG_EXPERT_BWD = orc.expert_bwd
+
+
+def _unstable_dispatch(topk_idx, E):
+    perm, inv, counts, off = _ORIG_DISPATCH(topk_idx, E)
+    for e in range(E):  # reverse every group: still grouped, no longer stable
+        perm[off[e]:off[e + 1]] = perm[off[e]:off[e + 1]][::-1].copy()
+    inv[perm] = np.arange(perm.size)
+    return perm, inv, counts, off
+
+
+def _transposed_wd_backward(sel_off, w_gate, w_up, w_down, *a, **kw):
+    wd = np.asarray(w_down)
+    # a mistake that keeps the shapes: reverse each W_down row
+    return _ORIG_EXPERT_BWD(sel_off, w_gate, w_up, wd[:, :, ::-1], *a, **kw)
+
+
+@pytest.mark.parametrize("planted", ["swiglu_sign", "score_alpha", "unstable", "wd_flip"])
+def test_planted_mistakes_are_caught(planted, monkeypatch):
+    if planted == "swiglu_sign":
+        monkeypatch.setattr(orc, "swiglu_grad", _wrong_swiglu_sign)
+        monkeypatch.setattr(oracle, "swiglu_grad", _wrong_swiglu_sign)
+        pins = [test_backward_matches_finite_differences_at_full_retention,
+                test_swiglu_grad_special_cases_and_derivative]
+    elif planted == "score_alpha":
+        monkeypatch.setattr(orc, "score", _score_without_alpha)
+        monkeypatch.setattr(oracle, "score", _score_without_alpha)
+        pins = [test_score_equals_bruteforce_frobenius_norm,
+                lambda: test_aggregate_error_relation_and_bound_eq19_20(0)]
+    elif planted == "unstable":
+        monkeypatch.setattr(orc, "dispatch_permute", _unstable_dispatch)
+        monkeypatch.setattr(oracle, "dispatch_permute", _unstable_dispatch)
+        pins = [test_reindex_worked_example,
+                lambda: test_dispatch_matches_python_stable_sort(7, 2, 5, 1)]
+    else:
+        monkeypatch.setattr(orc, "expert_bwd", _transposed_wd_backward)
+        pins = [test_backward_matches_finite_differences_at_full_retention]
+    for pin in pins:
+        with pytest.raises(AssertionError):
+            pin()
