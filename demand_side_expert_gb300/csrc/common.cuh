@@ -1,0 +1,119 @@
+// Shared host/device helpers of liblrm (validation, error word, vector I/O).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lrm.h"
+
+namespace lrm {
+
+constexpr size_t kWsHeaderBytes = 256;  // error word + reserved
+
+inline int32_t* error_word(void* ws) { return static_cast<int32_t*>(ws); }
+
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline int elem_bytes(int32_t dtype) { return dtype == LRM_BF16 ? 2 : 4; }
+
+// Validates the shape fields shared by every call. Returns LRM_OK or a code.
+inline lrm_status check_shape(const lrm_shape* s) {
+  if (!s) return LRM_ERR_INVALID_ARG;
+  if (s->T < 0 || s->D <= 0 || s->H <= 0 || s->E <= 0 || s->K <= 0)
+    return LRM_ERR_INVALID_ARG;
+  if (s->K > s->E) return LRM_ERR_INVALID_ARG;
+  if (s->dtype != LRM_F32 && s->dtype != LRM_BF16) return LRM_ERR_INVALID_ARG;
+  if ((int64_t)s->T * s->K >= (int64_t)1 << 31) return LRM_ERR_UNSUPPORTED;
+  if (s->D % 8 != 0 || s->H % 8 != 0) return LRM_ERR_UNSUPPORTED;
+  if (s->E > 1024) return LRM_ERR_UNSUPPORTED;
+  return LRM_OK;
+}
+
+size_t workspace_bytes(const lrm_shape* s);
+
+inline lrm_status check_ws(const lrm_shape* s, const void* ws, size_t ws_bytes) {
+  if (!ws) return LRM_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LRM_ERR_UNSUPPORTED;
+  if (ws_bytes < workspace_bytes(s)) return LRM_ERR_WORKSPACE;
+  return LRM_OK;
+}
+
+inline lrm_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
+}
+
+inline int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void flag_error(int32_t* err, int32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// 16-byte vector of activations: 8 bf16 or 4 floats, unpacked to floats.
+template <typename T>
+struct Vec16;
+
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    uint4 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+  }
+};
+
+template <>
+struct Vec16<float> {
+  static constexpr int kElems = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+}  // namespace lrm

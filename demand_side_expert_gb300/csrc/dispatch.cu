@@ -1,0 +1,281 @@
+// Forward dispatch permutation, row re-index, quota rule, workspace and the
+// device error word.
+//
+// Dispatch is a stable counting sort of the N = T*K pairs by expert id
+// ("Least-Loaded Expert Parallelism", Sec. 2.1 re-index and Alg. 4 sort of
+// the flattened indices; LRMoE Alg. 1 counts N_e). Three launches, no
+// inter-CTA waiting:
+//   1. per-chunk histogram (each CTA owns kChunk consecutive pairs),
+//   2. one CTA scans counts -> off and chunk bases (expert-major),
+//   3. each CTA replays its chunk warp by warp; inside a warp, lanes that
+//      share an expert are ranked with __match_any_sync, so positions follow
+//      ascending pair index (stability) without atomics on the output.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace lrm {
+
+constexpr int kDispThreads = 256;  // 8 warps
+constexpr int kDispWarps = kDispThreads / 32;
+constexpr int kPairsPerWarp = 256;
+constexpr int kChunk = kDispWarps * kPairsPerWarp;  // 2048 pairs per CTA
+
+inline int dispatch_chunks(int64_t N) {
+  return (int)std::max<int64_t>(1, (N + kChunk - 1) / kChunk);
+}
+
+inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+size_t workspace_bytes(const lrm_shape* s) {
+  const int64_t N = (int64_t)s->T * s->K;
+  const size_t chunk_tables = align256((size_t)2 * s->E * dispatch_chunks(N) * 4);
+  return kWsHeaderBytes + chunk_tables;
+}
+
+__device__ __forceinline__ int clamp_expert(int e, int E, int32_t* err) {
+  if (e < 0 || e >= E) {
+    flag_error(err, LRM_DEVERR_EXPERT_ID);
+    e = e < 0 ? 0 : E - 1;
+  }
+  return e;
+}
+
+// Warp-private histograms of one chunk: hist[w * E + e].
+__device__ __forceinline__ void chunk_histogram(const int32_t* __restrict__ idx,
+                                                int64_t N, int E, int32_t* hist,
+                                                int32_t* err) {
+  for (int i = threadIdx.x; i < kDispWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t base = (int64_t)blockIdx.x * kChunk + (int64_t)w * kPairsPerWarp;
+  for (int it = 0; it < kPairsPerWarp / 32; ++it) {
+    const int64_t p = base + it * 32 + lane;
+    const bool valid = p < N;
+    int e = valid ? clamp_expert(idx[p], E, err) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (valid && lane == __ffs(peers) - 1) hist[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kDispThreads)
+dispatch_hist_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int nblk,
+                     int32_t* __restrict__ chunk_hist, int32_t* err) {
+  extern __shared__ int32_t sh[];
+  chunk_histogram(idx, N, E, sh, err);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int w = 0; w < kDispWarps; ++w) s += sh[w * E + e];
+    chunk_hist[(int64_t)e * nblk + blockIdx.x] = s;
+  }
+}
+
+// Exclusive scan across the block (blockDim.x a multiple of 32, <= 1024).
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) warp_tot[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    int x = lane < nw ? warp_tot[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += t;
+    }
+    if (lane < nw) warp_tot[lane] = xi - x;
+    if (lane == 31) *total = xi;
+  }
+  __syncthreads();
+  const int r = warp_tot[w] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024)
+dispatch_scan_kernel(const int32_t* __restrict__ chunk_hist, int E, int nblk,
+                     int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
+                     int32_t* __restrict__ off) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int e = threadIdx.x;
+  int n = 0;
+  if (e < E)
+    for (int b = 0; b < nblk; ++b) n += chunk_hist[(int64_t)e * nblk + b];
+  const int excl = block_exclusive_scan(e < E ? n : 0, warp_tot, &total);
+  if (e < E) {
+    counts[e] = n;
+    off[e] = excl;
+    int run = excl;
+    for (int b = 0; b < nblk; ++b) {
+      chunk_base[(int64_t)e * nblk + b] = run;
+      run += chunk_hist[(int64_t)e * nblk + b];
+    }
+  }
+  if (threadIdx.x == 0) off[E] = total;
+}
+
+__global__ void __launch_bounds__(kDispThreads)
+dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int nblk,
+                        const int32_t* __restrict__ chunk_base,
+                        int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  extern __shared__ int32_t sh[];
+  int32_t* hist = sh;                       // [8][E]
+  int32_t* run = sh + kDispWarps * E;       // [8][E] next position per warp
+  chunk_histogram(idx, N, E, hist, nullptr);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int acc = chunk_base[(int64_t)e * nblk + blockIdx.x];
+    for (int w = 0; w < kDispWarps; ++w) {
+      run[w * E + e] = acc;
+      acc += hist[w * E + e];
+    }
+  }
+  __syncthreads();
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t base = (int64_t)blockIdx.x * kChunk + (int64_t)w * kPairsPerWarp;
+  for (int it = 0; it < kPairsPerWarp / 32; ++it) {
+    const int64_t p = base + it * 32 + lane;
+    const bool valid = p < N;
+    int e = -1;
+    if (valid) {
+      e = idx[p];
+      e = e < 0 ? 0 : (e >= E ? E - 1 : e);
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (valid) {
+      const int pos = run[w * E + e] + __popc(peers & lanemask_lt());
+      perm[pos] = (int32_t)p;
+      inv[p] = pos;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) run[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+__global__ void permute_rows_kernel(const int32_t* __restrict__ perm, int n_rows,
+                                    const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                    int64_t vec_per_row) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t pos = warp; pos < n_rows; pos += nwarps) {
+    const int p = perm[pos];
+    if (p < 0 || p >= n_rows) continue;
+    const uint4* s = src + (int64_t)p * vec_per_row;
+    uint4* d = dst + pos * vec_per_row;
+    for (int64_t c = lane; c < vec_per_row; c += 32) d[c] = ld_stream(s + c);
+  }
+}
+
+__global__ void quota_kernel(const int32_t* __restrict__ counts, int E, int num, int den,
+                             int cap, int32_t* __restrict__ quota) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int64_t n = counts[e];
+  int64_t q = ((int64_t)num * n + den - 1) / den;
+  if (cap > 0 && q > cap) q = cap;
+  quota[e] = (int32_t)q;
+}
+
+__global__ void clear_word_kernel(int32_t* w) { *w = 0; }
+
+}  // namespace lrm
+
+using namespace lrm;
+
+extern "C" size_t lrm_workspace_bytes(const lrm_shape* shape) {
+  if (check_shape(shape) != LRM_OK) return 0;
+  return workspace_bytes(shape);
+}
+
+extern "C" const char* lrm_status_string(lrm_status s) {
+  switch (s) {
+    case LRM_OK: return "LRM_OK";
+    case LRM_ERR_INVALID_ARG: return "LRM_ERR_INVALID_ARG";
+    case LRM_ERR_UNSUPPORTED: return "LRM_ERR_UNSUPPORTED";
+    case LRM_ERR_WORKSPACE: return "LRM_ERR_WORKSPACE";
+    case LRM_ERR_CUDA: return "LRM_ERR_CUDA";
+  }
+  return "LRM_ERR_UNKNOWN";
+}
+
+extern "C" lrm_status lrm_clear_device_error(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kWsHeaderBytes) return LRM_ERR_WORKSPACE;
+  clear_word_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(error_word(ws));
+  return launch_status();
+}
+
+extern "C" lrm_status lrm_get_device_error(const void* ws, size_t ws_bytes,
+                                           int32_t* code_out, void* stream) {
+  if (!ws || ws_bytes < kWsHeaderBytes) return LRM_ERR_WORKSPACE;
+  if (!code_out) return LRM_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LRM_ERR_CUDA;
+  if (cudaMemcpy(code_out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LRM_ERR_CUDA;
+  return LRM_OK;
+}
+
+extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* topk_idx,
+                                           int32_t* perm, int32_t* inv, int32_t* counts,
+                                           int32_t* off, void* ws, size_t ws_bytes,
+                                           void* stream) {
+  lrm_status st = check_shape(s);
+  if (st != LRM_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
+  const int64_t N = (int64_t)s->T * s->K;
+  if ((N > 0 && (!topk_idx || !perm || !inv)) || !counts || !off)
+    return LRM_ERR_INVALID_ARG;
+  cudaStream_t cs = (cudaStream_t)stream;
+  const int E = s->E;
+  const int nblk = dispatch_chunks(N);
+  int32_t* chunk_hist = reinterpret_cast<int32_t*>((char*)ws + kWsHeaderBytes);
+  int32_t* chunk_base = chunk_hist + (int64_t)E * nblk;
+  const size_t sh1 = (size_t)kDispWarps * E * 4;
+  const size_t sh3 = 2 * sh1;
+  if (sh3 > 48 * 1024) {
+    cudaFuncSetAttribute(dispatch_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sh1);
+    cudaFuncSetAttribute(dispatch_scatter_kernel,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh3);
+  }
+  dispatch_hist_kernel<<<nblk, kDispThreads, sh1, cs>>>(topk_idx, N, E, nblk, chunk_hist,
+                                                        error_word(ws));
+  dispatch_scan_kernel<<<1, 1024, 0, cs>>>(chunk_hist, E, nblk, chunk_base, counts, off);
+  dispatch_scatter_kernel<<<nblk, kDispThreads, sh3, cs>>>(topk_idx, N, E, nblk,
+                                                           chunk_base, perm, inv);
+  return launch_status();
+}
+
+extern "C" lrm_status lrm_permute_rows(const int32_t* perm, int32_t n_rows, const void* src,
+                                       void* dst, int64_t row_bytes, void* stream) {
+  if (n_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return LRM_ERR_INVALID_ARG;
+  if (n_rows == 0) return LRM_OK;
+  if (!perm || !src || !dst) return LRM_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return LRM_ERR_UNSUPPORTED;
+  const int64_t vec = row_bytes / 16;
+  const int64_t warps = std::min<int64_t>(n_rows, (int64_t)num_sms() * 64);
+  const int blocks = (int)((warps + 7) / 8);
+  permute_rows_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
+      perm, n_rows, (const uint4*)src, (uint4*)dst, vec);
+  return launch_status();
+}
+
+extern "C" lrm_status lrm_quota_from_rate(const int32_t* counts, int32_t E, int32_t num,
+                                          int32_t den, int32_t cap, int32_t* quota,
+                                          void* stream) {
+  if (E <= 0 || den <= 0 || num < 0 || num > den) return LRM_ERR_INVALID_ARG;
+  if (!counts || !quota) return LRM_ERR_INVALID_ARG;
+  quota_kernel<<<(E + 255) / 256, 256, 0, (cudaStream_t)stream>>>(counts, E, num, den, cap,
+                                                                  quota);
+  return launch_status();
+}

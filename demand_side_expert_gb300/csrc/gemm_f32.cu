@@ -1,0 +1,123 @@
+// FP32 variant of the four expert-backward products on CUDA cores.
+//
+// Same arithmetic as the tensor-core path (LRMoE Alg. 1 PackedExpertBackward
+// over each expert's retained rows; m_e read from sel_off on the device),
+// one thread per output element with a sequential FP32 dot product. It
+// serves FP32 layers, whose sizes are small; the BF16 path is the fast one.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lrm {
+
+constexpr int kF32Threads = 256;
+
+__device__ __forceinline__ int expert_of_row(const int32_t* sel_off, int E, int j) {
+  int lo = 0, hi = E;  // largest e with sel_off[e] <= j
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sel_off[mid] <= j) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// G1 + SwiGLU gradient: dab_c[j] = [da | db]
+__global__ void f32_g1_kernel(const int32_t* __restrict__ sel_off, int E, int D, int H,
+                              const float* __restrict__ dy_c, const float* __restrict__ w_down,
+                              const float* __restrict__ ab_c, float* __restrict__ dab_c) {
+  const int64_t M = sel_off[E];
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < M * H;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(o / H), h = (int)(o % H);
+    const int e = expert_of_row(sel_off, E, j);
+    const float* wd = w_down + ((int64_t)e * H + h) * D;
+    const float* dy = dy_c + (int64_t)j * D;
+    float dphi = 0.f;
+    for (int d = 0; d < D; ++d) dphi = fmaf(dy[d], wd[d], dphi);
+    const float a = ab_c[(int64_t)j * 2 * H + h];
+    const float b = ab_c[(int64_t)j * 2 * H + H + h];
+    const float s = 1.0f / (1.0f + expf(-a));
+    dab_c[(int64_t)j * 2 * H + h] = dphi * b * s * (1.0f + a * (1.0f - s));
+    dab_c[(int64_t)j * 2 * H + H + h] = dphi * a * s;
+  }
+}
+
+// G4: dx_c[j, d] = sum_h da[j,h] W_gate[e][d,h] + db[j,h] W_up[e][d,h]
+__global__ void f32_g4_kernel(const int32_t* __restrict__ sel_off, int E, int D, int H,
+                              const float* __restrict__ dab_c, const float* __restrict__ w_gate,
+                              const float* __restrict__ w_up, float* __restrict__ dx_c) {
+  const int64_t M = sel_off[E];
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < M * D;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(o / D), d = (int)(o % D);
+    const int e = expert_of_row(sel_off, E, j);
+    const float* wg = w_gate + ((int64_t)e * D + d) * H;
+    const float* wu = w_up + ((int64_t)e * D + d) * H;
+    const float* da = dab_c + (int64_t)j * 2 * H;
+    float acc = 0.f;
+    for (int h = 0; h < H; ++h) acc = fmaf(da[h], wg[h], acc);
+    for (int h = 0; h < H; ++h) acc = fmaf(da[H + h], wu[h], acc);
+    dx_c[(int64_t)j * D + d] = acc;
+  }
+}
+
+// G2: dW_down[e][h, d] = sum_{j in e} phi_c[j,h] dy_c[j,d]
+__global__ void f32_g2_kernel(const int32_t* __restrict__ sel_off, int E, int D, int H,
+                              const float* __restrict__ phi_c, const float* __restrict__ dy_c,
+                              float* __restrict__ dw_down) {
+  const int64_t total = (int64_t)E * H * D;
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(o / ((int64_t)H * D));
+    const int h = (int)((o / D) % H), d = (int)(o % D);
+    float acc = 0.f;
+    for (int j = sel_off[e]; j < sel_off[e + 1]; ++j)
+      acc = fmaf(phi_c[(int64_t)j * H + h], dy_c[(int64_t)j * D + d], acc);
+    dw_down[o] = acc;
+  }
+}
+
+// G3: dW_gate[e][d, n] / dW_up[e][d, n - H] = sum_{j in e} x_c[j,d] dab_c[j,n]
+__global__ void f32_g3_kernel(const int32_t* __restrict__ sel_off, int E, int D, int H,
+                              const float* __restrict__ x_c, const float* __restrict__ dab_c,
+                              float* __restrict__ dw_gate, float* __restrict__ dw_up) {
+  const int64_t total = (int64_t)E * D * 2 * H;
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(o / ((int64_t)D * 2 * H));
+    const int d = (int)((o / (2 * H)) % D), n = (int)(o % (2 * H));
+    float acc = 0.f;
+    for (int j = sel_off[e]; j < sel_off[e + 1]; ++j)
+      acc = fmaf(x_c[(int64_t)j * D + d], dab_c[(int64_t)j * 2 * H + n], acc);
+    float* out = n < H ? dw_gate : dw_up;
+    out[((int64_t)e * D + d) * H + (n < H ? n : n - H)] = acc;
+  }
+}
+
+lrm_status launch_bwd_f32(const BwdArgs& a) {
+  const lrm_shape* s = a.s;
+  const int D = s->D, H = s->H, E = s->E;
+  const int64_t N = (int64_t)s->T * s->K;
+  const int sms = num_sms();
+  auto grid = [&](int64_t work) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>((work + kF32Threads - 1) / kF32Threads,
+                                                       (int64_t)sms * 8));
+  };
+  cudaStream_t cs = a.stream;
+  const float* dy = (const float*)a.dy_c;
+  f32_g1_kernel<<<grid(N * H), kF32Threads, 0, cs>>>(a.sel_off, E, D, H, dy,
+                                                     (const float*)a.w_down,
+                                                     (const float*)a.ab_c, (float*)a.dab_c);
+  f32_g2_kernel<<<grid((int64_t)E * H * D), kF32Threads, 0, cs>>>(
+      a.sel_off, E, D, H, (const float*)a.phi_c, dy, a.dw_down);
+  f32_g3_kernel<<<grid((int64_t)E * D * 2 * H), kF32Threads, 0, cs>>>(
+      a.sel_off, E, D, H, (const float*)a.x_c, (const float*)a.dab_c, a.dw_gate, a.dw_up);
+  f32_g4_kernel<<<grid(N * D), kF32Threads, 0, cs>>>(a.sel_off, E, D, H,
+                                                     (const float*)a.dab_c,
+                                                     (const float*)a.w_gate,
+                                                     (const float*)a.w_up, a.dx_c);
+  return launch_status();
+}
+
+}  // namespace lrm

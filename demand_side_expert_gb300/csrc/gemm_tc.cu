@@ -1,0 +1,752 @@
+// Variable-size grouped GEMMs of the SwiGLU expert backward on tcgen05
+// tensor cores (BF16 operands, FP32 accumulation in tensor memory).
+//
+// LRMoE Alg. 1 (PackedExpertBackward) and Sec. 3.4: the four expert-backward
+// products run over each expert's retained rows only; the retained count m_e
+// is the row dimension of the data-gradient products (G1, G4) and the
+// reduction dimension of the weight-gradient products (G2, G3). Group sizes
+// are read from device memory (sel_off); nothing is padded:
+//   G1  dphi = dy_c W_down[e]^T   [m_e x H], epilogue: SwiGLU gradient
+//       -> dab_c = [da | db] (bf16); reads the saved ab_c rows.
+//   G2  dW_down[e] = phi_c^T dy_c   [H x D], reduction over m_e.
+//   G3  [dW_gate | dW_up][e] = x_c^T dab_c   [D x 2H], reduction over m_e.
+//   G4  dx_c = da W_gate[e]^T + db W_up[e]^T   [m_e x D] (fp32).
+//
+// Kernel shape (one CTA per SM, persistent over a device-computed tile list):
+//   warp 0    TMA producer: 128x64 A and 256x64 B tiles, 128-byte swizzle,
+//             4-stage ring of 48 KB stages guarded by mbarriers;
+//   warp 1    allocates 512 TMEM columns, one elected lane issues
+//             tcgen05.mma (M=128, N=256, K=16) into one of two 256-column
+//             accumulators; tcgen05.commit frees smem stages and hands
+//             finished accumulators to the epilogue;
+//   warps 2-5 epilogue: tcgen05.ld rows out of TMEM (one row per thread),
+//             fused SwiGLU gradient (G1) or masked FP32 stores.
+// Data-gradient tiles are cut at group ends (rows past m_e are computed and
+// masked on store). Weight-gradient tiles reduce over [sel_off[e],
+// sel_off[e+1]) in 64-row blocks; rows of the last block that belong to the
+// next group are zeroed in shared memory before the MMA reads them, and
+// 16-row slices past the group end are not issued. Experts with no retained
+// rows get zero weight gradients. Every mbarrier wait is bounded: on timeout
+// the CTA flags LRM_DEVERR_TIMEOUT, stops issuing, drains its copies and
+// MMAs, frees TMEM and returns.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lrm {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t BOX_BYTES = 64 * 64 * 2;  // one 64x64 MN-major box
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
+constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
+
+enum Mode { kG1 = 0, kG2 = 1, kG3 = 2, kG4 = 3 };
+
+struct Params {
+  int E, D, H;
+  int n_rows;  // row capacity of the compacted buffers
+  const int32_t* sel_off;
+  const __nv_bfloat16* ab_c;
+  __nv_bfloat16* dab_c;
+  float* out0;
+  float* out1;
+  int32_t* err;
+};
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity. Returns false when the
+// CTA is aborting or after kWaitNs; a timeout raises the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
+                                          volatile int* abort_flag, int32_t* err) {
+  if (mbar_try(b, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      *abort_flag = 1;
+      flag_error(err, LRM_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Whole-warp bounded wait: every lane polls, lane 0 alone decides to give up,
+// so the warp leaves together (tcgen05.ld and .sync.aligned ops that follow
+// need a converged warp). A completed phase stays observable until the
+// waiting warp itself lets the pipeline advance, so __all_sync terminates.
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity,
+                                          volatile int* abort_flag, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  uint64_t t0 = 0;
+  if (lane == 0) t0 = globaltimer();
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try(b, parity))) return true;
+    int give_up = 0;
+    if (lane == 0) {
+      if (*abort_flag) {
+        give_up = 1;
+      } else if (globaltimer() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        flag_error(err, LRM_DEVERR_TIMEOUT);
+        give_up = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+__device__ __forceinline__ void mbar_drain(uint64_t* b, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try(b, parity) && globaltimer() - t0 < kDrainNs) {
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   su32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          su32(bar))
+      : "memory");
+}
+// 32 TMEM lanes x 32 consecutive 32-bit columns; thread i gets lane (base+i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
+// start>>4 at [0,14), LBO>>4 at [16,30), SBO>>4 at [32,46), fixed 0b001 at
+// [46,49), swizzle mode 2 = 128B at [61,64)).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: FP32 accumulate, BF16 A and B,
+// operand majorness (0 = K-major, 1 = MN-major), N>>3 at [17,23), M>>4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) |
+         ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int MODE>
+struct Geo {
+  static constexpr bool kWgrad = (MODE == kG2 || MODE == kG3);
+};
+
+// ----------------------------------------------------------------------------
+// tile list
+// ----------------------------------------------------------------------------
+struct Tile {
+  int e;       // expert
+  int m0;      // dgrad: first compacted row; wgrad: first output row
+  int n0;      // first output column
+  int nkb;     // 64-wide K blocks
+  int valid;   // dgrad: rows of the tile inside the group; wgrad: rows of the last K block
+  int row0;    // wgrad: first compacted row of the group
+};
+
+struct Sched {
+  const int* goff;   // [E+1] group offsets (validated copy of sel_off)
+  const int* tpre;   // dgrad: [E+1] tile prefix
+  const int* order;  // wgrad: experts by retained rows, descending
+  int E, ntn, mtiles, kdim_blocks, total;
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile decode(const Sched& s, int tau) {
+  Tile t;
+  if constexpr (Geo<MODE>::kWgrad) {
+    const int per = s.mtiles * s.ntn;
+    const int r = tau / per, loc = tau - r * per;
+    t.e = s.order[r];
+    t.m0 = (loc / s.ntn) * BM;
+    t.n0 = (loc % s.ntn) * BN;
+    t.row0 = s.goff[t.e];
+    const int m = s.goff[t.e + 1] - t.row0;
+    t.nkb = (m + BK - 1) / BK;
+    t.valid = m - (t.nkb - 1) * BK;
+  } else {
+    int lo = 0, hi = s.E;  // largest e with tpre[e] <= tau
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s.tpre[mid] <= tau) lo = mid; else hi = mid;
+    }
+    t.e = lo;
+    const int loc = tau - s.tpre[lo];
+    const int mt = loc / s.ntn;
+    t.m0 = s.goff[lo] + mt * BM;
+    t.n0 = (loc % s.ntn) * BN;
+    t.valid = min(BM, s.goff[lo + 1] - t.m0);
+    t.nkb = s.kdim_blocks;
+    t.row0 = 0;
+  }
+  return t;
+}
+
+// ----------------------------------------------------------------------------
+// epilogues (one thread = one accumulator row, 32 columns per call)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&r)[32]) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                       __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+}
+__device__ __forceinline__ void zero_f32x32(float* dst) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// SwiGLU gradient of 32 columns h..h+31 of compacted row j.
+__device__ __forceinline__ void swiglu_epilogue(const Params& p, int64_t j, int h,
+                                                const uint32_t (&r)[32]) {
+  const int H = p.H;
+  const uint4* arow = reinterpret_cast<const uint4*>(p.ab_c + j * 2 * H + h);
+  const uint4* brow = reinterpret_cast<const uint4*>(p.ab_c + j * 2 * H + H + h);
+  uint4* darow = reinterpret_cast<uint4*>(p.dab_c + j * 2 * H + h);
+  uint4* dbrow = reinterpret_cast<uint4*>(p.dab_c + j * 2 * H + H + h);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float a[8], b[8], da[8], db[8];
+    Vec16<__nv_bfloat16>::unpack(arow[v], a);
+    Vec16<__nv_bfloat16>::unpack(brow[v], b);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float dphi = __uint_as_float(r[8 * v + u]);
+      const float s = 1.0f / (1.0f + __expf(-a[u]));
+      da[u] = dphi * b[u] * s * (1.0f + a[u] * (1.0f - s));
+      db[u] = dphi * a[u] * s;
+    }
+    darow[v] = Vec16<__nv_bfloat16>::pack(da);
+    dbrow[v] = Vec16<__nv_bfloat16>::pack(db);
+  }
+}
+
+// Output location of 32 consecutive accumulator columns (row, col); nullptr
+// when the chunk is outside the output (masked).
+template <int MODE>
+__device__ __forceinline__ float* out_ptr(const Params& p, const Tile& t, int row_local,
+                                          int col) {
+  if constexpr (MODE == kG4) {
+    if (row_local >= t.valid || col >= p.D) return nullptr;
+    return p.out0 + (int64_t)(t.m0 + row_local) * p.D + col;
+  } else if constexpr (MODE == kG2) {
+    const int h = t.m0 + row_local;
+    if (h >= p.H || col >= p.D) return nullptr;
+    return p.out0 + ((int64_t)t.e * p.H + h) * p.D + col;
+  } else if constexpr (MODE == kG3) {
+    const int d = t.m0 + row_local;
+    if (d >= p.D || col >= 2 * p.H) return nullptr;
+    if (col < p.H) return p.out0 + ((int64_t)t.e * p.D + d) * p.H + col;
+    return p.out1 + ((int64_t)t.e * p.D + d) * p.H + (col - p.H);
+  }
+  return nullptr;
+}
+
+// ----------------------------------------------------------------------------
+// the kernel
+// ----------------------------------------------------------------------------
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
+                    const __grid_constant__ CUtensorMap mapB,
+                    const __grid_constant__ CUtensorMap mapB2, const Params p) {
+  constexpr bool WG = Geo<MODE>::kWgrad;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* bad_flag = const_cast<int*>(abort_flag) + 1;
+  int* goff = bad_flag + 1;          // [E+1]
+  int* tab = goff + p.E + 1;         // dgrad: tpre[E+1]; wgrad: order[E]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E;
+
+  // --- set-up: validated group offsets, tile table, barriers, TMEM -------
+  if (tid == 0) {
+    *abort_flag = 0;
+    *bad_flag = 0;
+  }
+  __syncthreads();
+  const int nrows_cap = p.n_rows;
+  for (int i = tid; i <= E; i += kThreads) {
+    const int v = p.sel_off[i];
+    const int prev = i > 0 ? p.sel_off[i - 1] : 0;
+    goff[i] = v;
+    if (v < prev || (i == 0 && v != 0) || v > nrows_cap) *bad_flag = 1;
+  }
+  __syncthreads();
+  if (*bad_flag) {
+    for (int i = tid; i <= E; i += kThreads) goff[i] = 0;
+    if (tid == 0) flag_error(p.err, LRM_DEVERR_INDEX);
+  }
+  __syncthreads();
+
+  Sched sc;
+  sc.goff = goff;
+  sc.E = E;
+  if constexpr (MODE == kG1) {
+    sc.ntn = (p.H + BN - 1) / BN;
+    sc.kdim_blocks = p.D / BK;
+  } else if constexpr (MODE == kG4) {
+    sc.ntn = (p.D + BN - 1) / BN;
+    sc.kdim_blocks = 2 * p.H / BK;
+  } else if constexpr (MODE == kG2) {
+    sc.ntn = (p.D + BN - 1) / BN;
+    sc.mtiles = (p.H + BM - 1) / BM;
+  } else {
+    sc.ntn = (2 * p.H + BN - 1) / BN;
+    sc.mtiles = (p.D + BM - 1) / BM;
+  }
+  if constexpr (WG) {
+    // experts ordered by retained rows (descending, then by id): longest first
+    for (int e = tid; e < E; e += kThreads) {
+      const int m = goff[e + 1] - goff[e];
+      int rank = 0;
+      for (int f = 0; f < E; ++f) {
+        const int mf = goff[f + 1] - goff[f];
+        rank += (mf > m) || (mf == m && f < e);
+      }
+      tab[rank] = e;
+    }
+    sc.order = tab;
+    sc.total = E * sc.mtiles * sc.ntn;
+  } else {
+    if (warp == 0) {  // tile prefix over experts, 32 at a time
+      int carry = 0;
+      for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        const int tiles = e < E ? ((goff[e + 1] - goff[e] + BM - 1) / BM) * sc.ntn : 0;
+        int inc = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += t;
+        }
+        if (e < E) tab[e] = carry + inc - tiles;
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+      }
+      if (lane == 0) tab[E] = carry;
+    }
+    sc.tpre = tab;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&mapA);
+    prefetch_map(&mapB);
+    if (MODE == kG4) prefetch_map(&mapB2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if constexpr (!WG) sc.total = tab[E];
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ===================== TMA producer =====================
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool stop = false;
+      for (int tau = blockIdx.x; tau < sc.total && !stop; tau += gridDim.x) {
+        const Tile t = decode<MODE>(sc, tau);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err)) {
+            stop = true;
+            break;
+          }
+          uint8_t* a_s = stages + stage * STAGE_BYTES;
+          uint8_t* b_s = a_s + A_BYTES;
+          mbar_expect_tx(&full[stage], STAGE_BYTES);
+          if constexpr (MODE == kG1) {
+            tma_load_2d(a_s, &mapA, &full[stage], kb * BK, t.m0);
+            tma_load_3d(b_s, &mapB, &full[stage], kb * BK, t.n0, t.e);
+          } else if constexpr (MODE == kG4) {
+            tma_load_2d(a_s, &mapA, &full[stage], kb * BK, t.m0);
+            const int hb = p.H / BK;
+            if (kb < hb)
+              tma_load_3d(b_s, &mapB, &full[stage], kb * BK, t.n0, t.e);
+            else
+              tma_load_3d(b_s, &mapB2, &full[stage], (kb - hb) * BK, t.n0, t.e);
+          } else {
+            const int y = t.row0 + kb * BK;
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(a_s + i * BOX_BYTES, &mapA, &full[stage], t.m0 + 64 * i, y);
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(b_s + i * BOX_BYTES, &mapB, &full[stage], t.n0 + 64 * i, y);
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every issued copy must land before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ===================== MMA issuer =====================
+    constexpr uint32_t idesc = idesc_bf16(BM, BN, WG ? 1 : 0, WG ? 1 : 0);
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool stop = false, issued_any = false;
+    for (int tau = blockIdx.x; tau < sc.total && !stop; tau += gridDim.x) {
+      const Tile t = decode<MODE>(sc, tau);
+      if (t.nkb <= 0) continue;
+      if (!warp_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        if (!warp_wait(&full[stage], phase, abort_flag, p.err)) {
+          stop = true;
+          break;
+        }
+        uint8_t* a_s = stages + stage * STAGE_BYTES;
+        uint8_t* b_s = a_s + A_BYTES;
+        const int valid = (WG && kb == t.nkb - 1) ? t.valid : BK;
+        const int nks = (valid + 15) >> 4;
+        if constexpr (WG) {
+          if (valid & 15) {
+            // rows [valid, 16*nks) of this block belong to the next group (or
+            // lie past the retained rows): zero them in every box
+            const int zrows = 16 * nks - valid;
+            const int nboxes = (BM + BN) / 64;
+            for (int idx = lane; idx < zrows * nboxes * 8; idx += 32) {
+              const int c16 = idx & 7;
+              const int rz = (idx >> 3) % zrows;
+              const int bx = (idx >> 3) / zrows;
+              uint8_t* box = bx < BM / 64 ? a_s + bx * BOX_BYTES : b_s + (bx - BM / 64) * BOX_BYTES;
+              *reinterpret_cast<uint4*>(box + (valid + rz) * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+          }
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = su32(a_s), b_addr = su32(b_s);
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            if (ks < nks) {
+              uint64_t ad, bd;
+              if constexpr (WG) {  // MN-major: 16 K-rows = 2 x 1024 B per step
+                ad = sw128_desc(a_addr + ks * 2048, BOX_BYTES, 1024);
+                bd = sw128_desc(b_addr + ks * 2048, BOX_BYTES, 1024);
+              } else {  // K-major: 16 elements = 32 B per step
+                ad = sw128_desc(a_addr + ks * 32, 16, 1024);
+                bd = sw128_desc(b_addr + ks * 32, 16, 1024);
+              }
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty[stage]);
+        }
+        issued_any = true;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (stop) break;
+      if (lane == 0) umma_commit(&tfull[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    // all MMAs of this CTA must finish before TMEM is released
+    if (issued_any && lane == 0) {
+      umma_commit(drain);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ===================== epilogue (warps 2..5) =====================
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_local = q * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tau = blockIdx.x; tau < sc.total; tau += gridDim.x) {
+      const Tile t = decode<MODE>(sc, tau);
+      if (t.nkb <= 0) {  // expert without retained rows: zero weight gradient
+        if constexpr (WG) {
+          for (int c = 0; c < BN; c += 32) {
+            float* dst = out_ptr<MODE>(p, t, row_local, t.n0 + c);
+            if (dst) zero_f32x32(dst);
+          }
+        }
+        continue;
+      }
+      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c, r);
+        tmem_ld_wait();
+        if constexpr (MODE == kG1) {
+          const int h = t.n0 + c;
+          if (row_local < t.valid && h < p.H) swiglu_epilogue(p, (int64_t)t.m0 + row_local, h, r);
+        } else {
+          float* dst = out_ptr<MODE>(p, t, row_local, t.n0 + c);
+          if (dst) store_f32x32(dst, r);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// bf16 row-major [rows, cols] (rank 2) or [E, rows, cols] (rank 3), 128B swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int rank, uint64_t E, uint64_t rows,
+                     uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, E};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static size_t smem_bytes(int E) {
+  return 1024 + STAGES * STAGE_BYTES + 128 + 16 + (size_t)(2 * (E + 1) + 2) * 4;
+}
+
+template <int MODE>
+static lrm_status launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+                              const Params& p, int grid, cudaStream_t cs) {
+  const size_t smem = smem_bytes(p.E);
+  if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return LRM_ERR_CUDA;
+  grouped_gemm_kernel<MODE><<<grid, kThreads, smem, cs>>>(a, b, b2, p);
+  return launch_status();
+}
+
+}  // namespace tc
+
+lrm_status launch_bwd_tc(const BwdArgs& a) {
+  using namespace tc;
+  const lrm_shape* s = a.s;
+  const int D = s->D, H = s->H, E = s->E;
+  if (D % 64 != 0 || H % 64 != 0) return LRM_ERR_UNSUPPORTED;
+  const uint64_t N = (uint64_t)s->T * s->K;
+  const uint64_t rows = std::max<uint64_t>(N, 1);
+  CUtensorMap m_dy_k, m_dab_k, m_wdown, m_wgate, m_wup, m_phi_mn, m_dy_mn, m_x_mn, m_dab_mn;
+  bool ok = true;
+  // K-major operands of the data-gradient products
+  ok &= make_map(&m_dy_k, a.dy_c, 2, 1, rows, D, 64, BM);
+  ok &= make_map(&m_dab_k, a.dab_c, 2, 1, rows, 2 * H, 64, BM);
+  ok &= make_map(&m_wdown, a.w_down, 3, E, H, D, 64, BN);
+  ok &= make_map(&m_wgate, a.w_gate, 3, E, D, H, 64, BN);
+  ok &= make_map(&m_wup, a.w_up, 3, E, D, H, 64, BN);
+  // MN-major operands of the weight-gradient products (64 x 64 boxes)
+  ok &= make_map(&m_phi_mn, a.phi_c, 2, 1, rows, H, 64, 64);
+  ok &= make_map(&m_dy_mn, a.dy_c, 2, 1, rows, D, 64, 64);
+  ok &= make_map(&m_x_mn, a.x_c, 2, 1, rows, D, 64, 64);
+  ok &= make_map(&m_dab_mn, a.dab_c, 2, 1, rows, 2 * H, 64, 64);
+  if (!ok) return LRM_ERR_CUDA;
+
+  Params p;
+  p.E = E;
+  p.D = D;
+  p.H = H;
+  p.n_rows = (int)N;
+  p.sel_off = a.sel_off;
+  p.ab_c = reinterpret_cast<const __nv_bfloat16*>(a.ab_c);
+  p.dab_c = reinterpret_cast<__nv_bfloat16*>(a.dab_c);
+  p.err = a.err;
+  const int sms = num_sms();
+  const int64_t dg_tiles_n1 = ((int64_t)N / BM + E) * ((H + BN - 1) / BN);
+  const int64_t dg_tiles_n4 = ((int64_t)N / BM + E) * ((D + BN - 1) / BN);
+  const int64_t wg2 = (int64_t)E * ((H + BM - 1) / BM) * ((D + BN - 1) / BN);
+  const int64_t wg3 = (int64_t)E * ((D + BM - 1) / BM) * ((2 * H + BN - 1) / BN);
+  auto grid_of = [&](int64_t tiles) { return (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sms)); };
+
+  lrm_status st;
+  p.out0 = nullptr;
+  p.out1 = nullptr;
+  if ((st = launch_mode<kG1>(m_dy_k, m_wdown, m_wdown, p, grid_of(dg_tiles_n1), a.stream)) != LRM_OK)
+    return st;
+  p.out0 = a.dw_down;
+  if ((st = launch_mode<kG2>(m_phi_mn, m_dy_mn, m_dy_mn, p, grid_of(wg2), a.stream)) != LRM_OK)
+    return st;
+  p.out0 = a.dw_gate;
+  p.out1 = a.dw_up;
+  if ((st = launch_mode<kG3>(m_x_mn, m_dab_mn, m_dab_mn, p, grid_of(wg3), a.stream)) != LRM_OK)
+    return st;
+  p.out0 = a.dx_c;
+  p.out1 = nullptr;
+  return launch_mode<kG4>(m_dab_k, m_wgate, m_wup, p, grid_of(dg_tiles_n4), a.stream);
+}
+
+}  // namespace lrm

@@ -1,0 +1,115 @@
+"""Host orchestration of the recalibrated expert backward on one GPU.
+
+``RecalibratedExpertBackward`` owns the device buffers of one layer shape
+(allocated once through PyTorch, reused every step) and issues the C-ABI
+calls of liblrm in order on one CUDA stream:
+
+  lrm_dispatch_permute -> lrm_quota_from_rate -> lrm_score ->
+  lrm_select_quota -> lrm_compact -> lrm_expert_bwd_grouped
+
+Every step of the path runs in liblrm's kernels; this class only allocates,
+passes pointers and copies host buffers in and out (``run_host``).
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import lrm
+
+_TORCH_DTYPE = {lrm.LRM_F32: torch.float32, lrm.LRM_BF16: torch.bfloat16}
+
+
+def dtype_code(name: str) -> int:
+    return {"f32": lrm.LRM_F32, "bf16": lrm.LRM_BF16}[name]
+
+
+class RecalibratedExpertBackward:
+    """Buffers + call sequence for one (T, D, H, E, K, dtype) layer shape."""
+
+    def __init__(self, T: int, D: int, H: int, E: int, K: int, dtype: str = "bf16",
+                 device: str | torch.device = "cuda"):
+        self.T, self.D, self.H, self.E, self.K = T, D, H, E, K
+        self.N = T * K
+        self.dtype_code = dtype_code(dtype)
+        self.tdtype = _TORCH_DTYPE[self.dtype_code]
+        self.shape = lrm.make_shape(T, D, H, E, K, self.dtype_code)
+        dev = torch.device(device)
+        self.device = dev
+        i32, f32, dt = torch.int32, torch.float32, self.tdtype
+        N, rows = self.N, max(self.N, 1)
+
+        def empty(*shape, dtype):
+            return torch.empty(*shape, dtype=dtype, device=dev)
+
+        self.ws_bytes = lrm.lrm_workspace_bytes(self.shape)
+        if self.ws_bytes == 0:
+            raise lrm.LrmError("lrm_workspace_bytes", lrm.LRM_ERR_INVALID_ARG)
+        self.ws = empty(self.ws_bytes, dtype=torch.uint8)
+        self.perm, self.inv = empty(rows, dtype=i32), empty(rows, dtype=i32)
+        self.counts, self.off = empty(E, dtype=i32), empty(E + 1, dtype=i32)
+        self.quota = empty(E, dtype=i32)
+        self.score = empty(rows, dtype=f32)
+        self.keep = empty(rows, dtype=torch.uint8)
+        self.sel_off, self.sel_pos = empty(E + 1, dtype=i32), empty(rows, dtype=i32)
+        self.dy_c, self.x_c = empty(rows, D, dtype=dt), empty(rows, D, dtype=dt)
+        self.ab_c, self.phi_c = empty(rows, 2 * H, dtype=dt), empty(rows, H, dtype=dt)
+        self.tok_c, self.row_of_pos = empty(rows, dtype=i32), empty(rows, dtype=i32)
+        self.dab_c, self.dx_c = empty(rows, 2 * H, dtype=dt), empty(rows, D, dtype=f32)
+        self.dw_gate, self.dw_up = empty(E, D, H, dtype=f32), empty(E, D, H, dtype=f32)
+        self.dw_down = empty(E, H, D, dtype=f32)
+        self.dx = empty(max(T, 1), D, dtype=f32)
+        lrm.lrm_clear_device_error(self.ws, self.ws_bytes)
+        del N
+
+    # -- forward side -------------------------------------------------------
+    def dispatch(self, topk_idx, stream=None):
+        lrm.lrm_dispatch_permute(self.shape, topk_idx, self.perm, self.inv, self.counts,
+                                 self.off, self.ws, self.ws_bytes, stream)
+
+    def to_dispatch_order(self, rows_by_pair: torch.Tensor, stream=None) -> torch.Tensor:
+        """Lay per-pair rows out in dispatch order with the current perm."""
+        out = torch.empty_like(rows_by_pair)
+        row_bytes = rows_by_pair[0].numel() * rows_by_pair.element_size()
+        lrm.lrm_permute_rows(self.perm, self.N, rows_by_pair, out, row_bytes, stream)
+        return out
+
+    # -- backward -----------------------------------------------------------
+    def quota_from_rate(self, num: int, den: int, cap: int = 0, stream=None):
+        lrm.lrm_quota_from_rate(self.counts, self.E, num, den, cap, self.quota, stream)
+
+    def score_select_compact(self, alpha, x, g, ab, phi, stream=None):
+        s, w, wb = self.shape, self.ws, self.ws_bytes
+        lrm.lrm_score(s, g, phi, alpha, self.inv, self.score, w, wb, stream)
+        lrm.lrm_select_quota(s, self.score, self.off, self.quota, self.keep, self.sel_off,
+                             self.sel_pos, w, wb, stream)
+        lrm.lrm_compact(s, self.perm, self.keep, self.sel_off, self.sel_pos, alpha, x, g, ab,
+                        phi, self.dy_c, self.x_c, self.ab_c, self.phi_c, self.tok_c,
+                        self.row_of_pos, w, wb, stream)
+
+    def expert_bwd(self, w_gate, w_up, w_down, stream=None):
+        lrm.lrm_expert_bwd_grouped(
+            self.shape, self.sel_off, w_gate, w_up, w_down, self.dy_c, self.x_c, self.ab_c,
+            self.phi_c, self.inv, self.row_of_pos, self.dab_c, self.dx_c, self.dw_gate,
+            self.dw_up, self.dw_down, self.dx, self.ws, self.ws_bytes, stream)
+
+    def step(self, topk_idx, alpha, x, g, ab, phi, w_gate, w_up, w_down, rate=(1, 1),
+             cap: int = 0, quota: torch.Tensor | None = None, stream=None):
+        """One pass of the whole path. ab / phi are in dispatch order."""
+        self.dispatch(topk_idx, stream)
+        if quota is None:
+            self.quota_from_rate(rate[0], rate[1], cap, stream)
+        else:
+            self.quota.copy_(quota)
+        self.score_select_compact(alpha, x, g, ab, phi, stream)
+        self.expert_bwd(w_gate, w_up, w_down, stream)
+
+    def device_error(self, stream=None) -> int:
+        return lrm.lrm_get_device_error(self.ws, self.ws_bytes, stream)
+
+    def clear_device_error(self, stream=None):
+        lrm.lrm_clear_device_error(self.ws, self.ws_bytes, stream)
+
+    @property
+    def retained_rows(self) -> int:
+        return int(self.sel_off[self.E].item())

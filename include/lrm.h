@@ -1,0 +1,222 @@
+/*
+ * lrm.h -- C ABI of the recalibrated MoE expert backward on one GB300 GPU.
+ *
+ * The path follows "LRMoE: Demand-Side Load Re-Calibration for Efficient MoE
+ * Training on Memory-Constrained Nodes" (arXiv 2610.37720) on a single GPU:
+ *   forward dispatch permutation -> LRM score of every routed pair ->
+ *   per-expert top-q selection -> physical compaction -> SwiGLU expert
+ *   backward as variable-size grouped GEMMs over the retained rows only.
+ * Multi-GPU routing, replicas, all-to-all and the CPU offload queue of the
+ * paper are not part of this library.
+ *
+ * Notation: T tokens, D model dim, H expert FFN dim, E experts, K routed
+ * experts per token, N = T*K routed pairs; pair index p = t*K + k.
+ * "Dispatch order" lists the pairs grouped by expert (expert-major), inside a
+ * group by ascending p.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated; the
+ *    library never allocates or frees memory and keeps no global state
+ *    (calls on different streams are independent).
+ *  - All calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = legacy default stream) and never synchronise the host, except
+ *    lrm_get_device_error.
+ *  - Row-major contiguous layouts. Floating-point activations and weights
+ *    (x, g, ab, phi, W_*, dy_c, x_c, ab_c, phi_c, dab_c) have the element type
+ *    of lrm_shape.dtype (LRM_BF16: bfloat16, LRM_F32: float); routing weights,
+ *    scores and all gradients in float32; indices int32.
+ *  - Every pointer must be 16-byte aligned and D, H multiples of 8, else
+ *    LRM_ERR_UNSUPPORTED. The BF16 grouped backward also needs D and H to be
+ *    multiples of 64.
+ *  - Argument errors are returned before anything is launched. A failed
+ *    launch returns LRM_ERR_CUDA. Bad DATA found on the device (an expert id
+ *    outside [0, E), a quota outside [0, n_e], an index out of range, a
+ *    pipeline wait that timed out) never traps: the kernel clamps or skips,
+ *    ORs an LRM_DEVERR_* bit into the device error word kept in the first 4
+ *    bytes of the caller's workspace, and the call returns LRM_OK; read the
+ *    word with lrm_get_device_error.
+ *  - ws / ws_bytes: caller-owned device workspace of at least
+ *    lrm_workspace_bytes(shape) bytes, 256-byte aligned. Clear its error word
+ *    once with lrm_clear_device_error before first use.
+ */
+#ifndef LRM_H_
+#define LRM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lrm_status {
+  LRM_OK = 0,
+  LRM_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size */
+  LRM_ERR_UNSUPPORTED = 2, /* alignment / dimension not supported */
+  LRM_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  LRM_ERR_CUDA = 4         /* a CUDA launch or runtime call failed */
+} lrm_status;
+
+typedef enum lrm_dtype { LRM_F32 = 0, LRM_BF16 = 1 } lrm_dtype;
+
+/* Layer shape. dtype is an lrm_dtype. N = T*K must be < 2^31. */
+typedef struct lrm_shape {
+  int32_t T, D, H, E, K;
+  int32_t dtype;
+} lrm_shape;
+
+/* Bits of the device error word. */
+#define LRM_DEVERR_EXPERT_ID 1 /* topk_idx outside [0,E): clamped          */
+#define LRM_DEVERR_QUOTA 2     /* quota outside [0,n_e]: clamped           */
+#define LRM_DEVERR_INDEX 4     /* inv / perm / sel_pos out of range: row skipped */
+#define LRM_DEVERR_TIMEOUT 8   /* a GEMM pipeline wait gave up: outputs invalid */
+
+/* Bytes of workspace every call of this shape needs (host only, pure). */
+size_t lrm_workspace_bytes(const lrm_shape* shape);
+
+/* Zero the device error word (first 4 bytes of ws). Async on stream. */
+lrm_status lrm_clear_device_error(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then copy the device error word into *code_out. */
+lrm_status lrm_get_device_error(const void* ws, size_t ws_bytes,
+                                int32_t* code_out, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* lrm_status_string(lrm_status status);
+
+/*
+ * Forward dispatch permutation: a stable counting sort of the pairs by
+ * expert id. "Least-Loaded Expert Parallelism" (LLEP) Sec. 2.1 re-index
+ * (tokens [a,b,c,d] routed to experts [2,6,2,1] become [d,a,c,b]) and LLEP
+ * Alg. 4 sort of the flattened indices; LRMoE Alg. 1 forward admission
+ * counts N_e = |P_e|.
+ *   topk_idx [T,K] int32 : expert of pair p = t*K+k (read).
+ *   perm     [N]   int32 : perm[pos] = p, dispatch position -> pair (written).
+ *   inv      [N]   int32 : inv[p] = pos (written).
+ *   counts   [E]   int32 : n_e (written).
+ *   off      [E+1] int32 : exclusive prefix of counts, off[E] = N (written).
+ * Ids outside [0,E) are clamped into range and flag LRM_DEVERR_EXPERT_ID.
+ */
+lrm_status lrm_dispatch_permute(const lrm_shape* shape, const int32_t* topk_idx,
+                                int32_t* perm, int32_t* inv, int32_t* counts,
+                                int32_t* off, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/*
+ * Row re-index into dispatch order, dst[pos] = src[perm[pos]] for
+ * pos < n_rows (LLEP Sec. 2.1: B' is B with its rows taken in dispatch
+ * order). row_bytes must be a positive multiple of 16; src and dst must not
+ * overlap. Rows whose perm entry is outside [0, n_rows) are left untouched.
+ */
+lrm_status lrm_permute_rows(const int32_t* perm, int32_t n_rows, const void* src,
+                            void* dst, int64_t row_bytes, void* stream);
+
+/*
+ * Per-expert retention quota q_e = min(ceil(num/den * n_e), cap), computed
+ * in exact integer arithmetic; cap <= 0 means no cap. LRMoE Sec. 3.1: quotas
+ * satisfy 0 <= K_e <= N_e with retention rate rho = sum_e K_e / N, fixed for
+ * the invocation. Needs 0 <= num <= den, den > 0.
+ *   counts [E] int32 (read), quota [E] int32 (written).
+ */
+lrm_status lrm_quota_from_rate(const int32_t* counts, int32_t E, int32_t num,
+                               int32_t den, int32_t cap, int32_t* quota,
+                               void* stream);
+
+/*
+ * Load Recalibration Metric of every routed pair, LRMoE Sec. 3.2 Prop. 3.1
+ * Eq. 3 and Sec. 7.1 Eq. 12: R_u = alpha_u^2 * ||g_t||^2 * ||phi_u||^2, the
+ * squared Frobenius norm of the pair's rank-one FC2 weight-gradient
+ * contribution (alpha_u g_t) phi_u^T; g_t is the cotangent at the MoE output
+ * before the routing weight (Sec. 7.1 Eq. 5). FP32 accumulation.
+ *   g     [T,D] dtype          : output cotangent (read).
+ *   phi   [N,H] dtype          : saved FC2 input, dispatch order (read).
+ *   alpha [T,K] float          : routing weights (read).
+ *   inv   [N]   int32          : from lrm_dispatch_permute (read).
+ *   score [N]   float          : R in dispatch order (written).
+ */
+lrm_status lrm_score(const lrm_shape* shape, const void* g, const void* phi,
+                     const float* alpha, const int32_t* inv, float* score,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Per-expert top-q selection, LRMoE Alg. 1 (TopK per expert) and Sec. 7.2
+ * Prop. 7.1 (keeping the largest scores inside each expert is optimal for
+ * fixed per-expert quotas). Inside each segment [off[e], off[e+1]) the q_e
+ * largest scores are kept; equal scores are broken by the lower pair index,
+ * which inside a segment is the lower dispatch position. Scores must be
+ * non-negative and not NaN (they are sums of squares).
+ *   score   [N]   float (read), off [E+1] int32 (read), quota [E] int32 (read).
+ *   keep    [N]   uint8 : 1 if retained, dispatch order (written).
+ *   sel_off [E+1] int32 : exclusive prefix of the quotas (written).
+ *   sel_pos [N]   int32 : capacity N; the first M = sel_off[E] entries are
+ *                         the retained dispatch positions, ascending inside
+ *                         each expert (written).
+ * Quotas outside [0, n_e] are clamped and flag LRM_DEVERR_QUOTA.
+ */
+lrm_status lrm_select_quota(const lrm_shape* shape, const float* score,
+                            const int32_t* off, const int32_t* quota,
+                            uint8_t* keep, int32_t* sel_off, int32_t* sel_pos,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Physical compaction, LRMoE Sec. 3.1 (compact runtime) and Sec. 3.4 Fig. 4:
+ * retained gradient rows and their saved state are gathered into contiguous
+ * expert-major segments, with no zero-masked rows. For retained row
+ * j < M = sel_off[E]: i = sel_pos[j], p = perm[i], t = p / K:
+ *   dy_c[j]  = alpha[p] * g[t]   (product in float32, rounded once to dtype)
+ *   x_c[j]   = x[t],  ab_c[j] = ab[i],  phi_c[j] = phi[i],  tok_c[j] = t
+ *   row_of_pos[i] = j, and -1 at every position with keep[i] == 0.
+ * Inputs: perm [N], keep [N], sel_off [E+1], sel_pos [N], alpha [T,K],
+ *   x [T,D], g [T,D], ab [N,2H] (gate|up pre-activations, dispatch order),
+ *   phi [N,H] (dispatch order).
+ * Outputs (capacity N rows each, first M written): dy_c [N,D], x_c [N,D],
+ *   ab_c [N,2H], phi_c [N,H], tok_c [N] int32; row_of_pos [N] int32.
+ */
+lrm_status lrm_compact(const lrm_shape* shape, const int32_t* perm,
+                       const uint8_t* keep, const int32_t* sel_off,
+                       const int32_t* sel_pos, const float* alpha, const void* x,
+                       const void* g, const void* ab, const void* phi, void* dy_c,
+                       void* x_c, void* ab_c, void* phi_c, int32_t* tok_c,
+                       int32_t* row_of_pos, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
+ * SwiGLU expert backward over the retained rows, LRMoE Alg. 1
+ * (PackedExpertBackward) and Sec. 3.4: four variable-size grouped products
+ * per expert e over its m_e = sel_off[e+1] - sel_off[e] compacted rows J
+ * (m_e is the row dimension of the data-gradient products and the reduction
+ * dimension of the weight-gradient products; no padding):
+ *   dphi       = dy_c[J] W_down[e]^T,  then the SwiGLU gradient
+ *                da = dphi*b*s*(1 + a*(1-s)), db = dphi*a*s, s = sigmoid(a),
+ *                (a, b) = ab_c[J] halves  -> dab_c[J] = [da | db]   (dtype)
+ *   dW_down[e] = phi_c[J]^T dy_c[J]                               (H x D)
+ *   dW_gate[e] = x_c[J]^T da,  dW_up[e] = x_c[J]^T db             (D x H)
+ *   dx_c[J]    = da W_gate[e]^T + db W_up[e]^T                    (float32)
+ * then the scatter back to tokens (Sec. 3.1: zero-initialised dense buffer):
+ *   dx[t] = sum over kept slots k, ascending, of dx_c[row_of_pos[inv[t*K+k]]]
+ * (deterministic, no atomics). BF16 runs on tcgen05 tensor cores with FP32
+ * accumulation in tensor memory; F32 runs on CUDA cores.
+ *   w_gate, w_up [E,D,H] dtype; w_down [E,H,D] dtype (read).
+ *   dy_c, x_c [N,D]; ab_c [N,2H]; phi_c [N,H]  (read, first M rows used).
+ *   inv [N], row_of_pos [N] int32 (read).
+ *   dab_c [N,2H] dtype, dx_c [N,D] float : intermediates (first M rows written).
+ *   dw_gate, dw_up [E,D,H] float; dw_down [E,H,D] float : OVERWRITTEN
+ *     (zero for experts with no retained rows).
+ *   dx [T,D] float : overwritten.
+ * Pipeline waits are bounded; a timeout flags LRM_DEVERR_TIMEOUT.
+ */
+lrm_status lrm_expert_bwd_grouped(const lrm_shape* shape, const int32_t* sel_off,
+                                  const void* w_gate, const void* w_up,
+                                  const void* w_down, const void* dy_c,
+                                  const void* x_c, const void* ab_c,
+                                  const void* phi_c, const int32_t* inv,
+                                  const int32_t* row_of_pos, void* dab_c,
+                                  float* dx_c, float* dw_gate, float* dw_up,
+                                  float* dw_down, float* dx, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRM_H_ */

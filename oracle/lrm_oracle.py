@@ -293,24 +293,25 @@ def expert_bwd(sel_off, w_gate, w_up, w_down, dy_c, x_c, ab_c, phi_c,
             "dab_c": dab_c, "dx_c": dx_c}
 
 
-def expert_bwd_rows(rows, sel_off, w_gate, w_up, w_down, dy_c, ab_c):
+def expert_bwd_rows(rows, sel_off, w_gate, w_up, w_down, dy_rows, ab_rows):
     """Data-gradient rows only (dab_c[j], dx_c[j]) for a list of compacted rows.
 
-    Same arithmetic as ``expert_bwd`` restricted to the rows asked for; each
-    row's expert is the segment of sel_off that holds it. Used to check
-    sampled rows of full-size runs one by one.
+    Same arithmetic as ``expert_bwd`` restricted to the rows asked for:
+    ``rows`` are compacted row indices j (each row's expert is the segment of
+    sel_off that holds it) and dy_rows[n], ab_rows[n] hold dy_c[rows[n]],
+    ab_c[rows[n]]. Used to check sampled rows of full-size runs one by one.
     """
     sel_off = _i64(sel_off)
     wg, wu, wd = _f64(w_gate), _f64(w_up), _f64(w_down)
     H = wg.shape[2]
     rows = _i64(rows)
+    dy, abr = _f64(dy_rows), _f64(ab_rows)
     dab = np.zeros((rows.shape[0], 2 * H), dtype=F64)
     dxc = np.zeros((rows.shape[0], wg.shape[1]), dtype=F64)
     for n, j in enumerate(rows):
         e = int(np.searchsorted(sel_off, j, side="right") - 1)
-        dphi = _f64(dy_c[j]) @ wd[e].T
-        abj = _f64(ab_c[j])
-        da, db = swiglu_grad(dphi, abj[:H], abj[H:])
+        dphi = dy[n] @ wd[e].T
+        da, db = swiglu_grad(dphi, abr[n, :H], abr[n, H:])
         dab[n, :H], dab[n, H:] = da, db
         dxc[n] = da @ wg[e].T + db @ wu[e].T
     return dab, dxc

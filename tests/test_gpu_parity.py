@@ -1,0 +1,297 @@
+"""Element-by-element parity of the CUDA path with the CPU oracle (GPU).
+
+Sizes here span several 128 x 256 tiles per expert with ragged tails in
+every dimension (rows per group, K blocks of the weight-gradient products,
+N tiles), plus the degenerate cases: empty and single-row experts, a group
+holding every token, zero and full retention, capped quotas, T = 0, bad
+expert ids and oversize quotas (flagged on the device, never trapped).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import generate, get_config
+
+from parity_util import (check_backward, check_compaction, check_dispatch, check_scores,
+                         check_selection, check_set_agreement, numpy_inputs, rel_fro, run_gpu,
+                         to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    from demand_side_expert_gb300 import lrm  # noqa: F401  (liblrm.so must load)
+    return torch.device("cuda:0")
+
+
+def _pipe(cfg, dev):
+    from demand_side_expert_gb300 import RecalibratedExpertBackward
+    return RecalibratedExpertBackward(cfg.T, cfg.D, cfg.H, cfg.E, cfg.K, cfg.dtype, dev)
+
+
+def _to(inp, dev):
+    return {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+
+
+def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None):
+    """Every step of the path against the oracle on one seeded layer."""
+    inp_cpu = generate(cfg, device="cpu", seed=seed)
+    inp = _to(inp_cpu, dev)
+    pipe = _pipe(cfg, dev)
+    q_t = None if quota is None else torch.as_tensor(quota, dtype=torch.int32, device=dev)
+    run_gpu(pipe, inp, rate, cap, q_t)
+    assert pipe.device_error() == 0
+    nin = numpy_inputs(inp_cpu)
+    perm, inv, counts, off = check_dispatch(pipe, nin["topk_idx"], cfg.E)
+    ab = oracle.lrm_oracle.permute_rows(nin["ab_pair"], perm)
+    phi = oracle.lrm_oracle.permute_rows(nin["phi_pair"], perm)
+    assert np.array_equal(to_np(pipe.quota),
+                          oracle.quota_from_rate(counts, rate[0], rate[1], cap)
+                          if quota is None else np.asarray(quota))
+    qv = to_np(pipe.quota).astype(np.int64)
+    ref_score = oracle.score(nin["g"], phi, nin["alpha"], perm, cfg.K)
+    N = cfg.N
+    check_scores(to_np(pipe.score)[:N], ref_score)
+    keep, sel_off, sel_pos = check_selection(pipe, perm, off, qv)
+    check_set_agreement(keep, ref_score, off, qv)
+    c = check_compaction(pipe, nin, perm, sel_off, sel_pos, ab, phi, cfg.K, cfg.dtype)
+    errs = check_backward(pipe, nin, c, sel_off, inv, cfg.T, cfg.K, cfg.dtype)
+    return pipe, errs
+
+
+# ---------------------------------------------------------------------------
+def test_tiny_fp32_layer(dev):
+    full_parity(get_config("tiny"), dev, (1, 2))
+
+
+@pytest.mark.parametrize("rate", [(1, 2), (3, 5), (1, 4)])
+def test_bf16_ragged_tiles(dev, rate):
+    # H=192: G1 N tile and G2 M tile ragged; 2H=384 ragged in G3; m_e ~ 160
+    # rows: several row tiles and a K tail that is not a multiple of 16
+    cfg = get_config("qwen3-30b-a3b-t4k", T=1024, D=320, H=192, E=12, K=3)
+    full_parity(cfg, dev, rate)
+
+
+def test_bf16_wide_layer_many_experts(dev):
+    cfg = get_config("glm45-106b-a12b-t16k", T=768, D=512, H=320, E=24, K=4)
+    full_parity(cfg, dev, (3, 4))
+
+
+def test_fp32_wider_layer(dev):
+    cfg = get_config("tiny", T=200, D=48, H=40, E=6, K=3)
+    full_parity(cfg, dev, (3, 5))
+
+
+def test_stress_edge_groups(dev):
+    # dead experts, single-row experts, near-full experts and a capped quota
+    cfg = get_config("stress-e256", T=2048, D=256, H=128)
+    inp = generate(cfg, device="cpu")
+    counts = np.bincount(inp["topk_idx"].reshape(-1).numpy(), minlength=cfg.E)
+    assert (counts == 0).sum() >= 16 and (counts == 1).sum() >= 1
+    cap = 100  # below the hot experts' ceil(n/2)
+    full_parity(cfg, dev, (1, 2), cap=cap)
+
+
+def test_explicit_quotas_and_extremes(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=300, D=128, H=64, E=10, K=2)
+    inp = generate(cfg, device="cpu")
+    counts = np.bincount(inp["topk_idx"].reshape(-1).numpy(), minlength=cfg.E)
+    quota = counts.copy()
+    quota[0] = 0                 # nothing kept
+    quota[1] = min(1, counts[1])  # one row
+    quota[2] = counts[2]         # everything kept
+    quota[3:] = counts[3:] // 3
+    full_parity(cfg, dev, (1, 1), quota=quota.astype(np.int32))
+
+
+def test_zero_retention(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=256, D=128, H=64, E=8, K=2)
+    pipe, _ = full_parity(cfg, dev, (0, 1))
+    assert pipe.retained_rows == 0
+    assert float(pipe.dw_down.abs().max()) == 0.0 and float(pipe.dx.abs().max()) == 0.0
+
+
+def test_empty_layer(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=0, D=128, H=64, E=4, K=2)
+    from workloads.configs import LayerConfig  # noqa: F401
+    pipe = _pipe(cfg, dev)
+    z = torch.zeros(0, 2, dtype=torch.int32, device=dev)
+    pipe.dispatch(z)
+    pipe.quota_from_rate(1, 2)
+    pipe.score_select_compact(torch.zeros(0, 2, device=dev),
+                              torch.zeros(0, 128, dtype=torch.bfloat16, device=dev),
+                              torch.zeros(0, 128, dtype=torch.bfloat16, device=dev),
+                              torch.zeros(1, 128, dtype=torch.bfloat16, device=dev),
+                              torch.zeros(1, 64, dtype=torch.bfloat16, device=dev))
+    w = torch.zeros(4, 128, 64, dtype=torch.bfloat16, device=dev)
+    pipe.expert_bwd(w, w, torch.zeros(4, 64, 128, dtype=torch.bfloat16, device=dev))
+    torch.cuda.synchronize()
+    assert pipe.device_error() == 0
+    assert to_np(pipe.off).tolist() == [0] * 5
+    assert to_np(pipe.sel_off).tolist() == [0] * 5
+    assert float(pipe.dw_gate.abs().max()) == 0.0
+
+
+def test_full_retention_bitwise_equals_uncompacted_run(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=640, D=256, H=128, E=8, K=2)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    ab, phi = run_gpu(pipe, inp, (1, 1))
+    N = cfg.N
+    perm = pipe.perm[:N].long()
+    assert torch.equal(pipe.sel_pos[:N].long(), torch.arange(N, device=dev))
+    assert torch.equal(pipe.row_of_pos[:N].long(), torch.arange(N, device=dev))
+    assert torch.equal(pipe.ab_c[:N], ab) and torch.equal(pipe.phi_c[:N], phi)
+    # the unpruned backward run directly on the uncompacted dispatch-order rows
+    dy = (inp["alpha"].reshape(-1)[perm][:, None] * inp["g"][perm // cfg.K].float()).to(
+        torch.bfloat16)
+    xs = inp["x"][perm // cfg.K].contiguous()
+    assert torch.equal(pipe.dy_c[:N], dy) and torch.equal(pipe.x_c[:N], xs)
+    outs = {k: getattr(pipe, k).clone() for k in ("dw_gate", "dw_up", "dw_down", "dx")}
+    from demand_side_expert_gb300 import lrm
+    ident = torch.arange(N, dtype=torch.int32, device=dev)
+    dab = torch.empty_like(pipe.dab_c)
+    dxc = torch.empty_like(pipe.dx_c)
+    res = {k: torch.empty_like(v) for k, v in outs.items()}
+    lrm.lrm_expert_bwd_grouped(pipe.shape, pipe.off, inp["w_gate"], inp["w_up"],
+                               inp["w_down"], dy, xs, ab, phi, pipe.inv, ident, dab, dxc,
+                               res["dw_gate"], res["dw_up"], res["dw_down"], res["dx"],
+                               pipe.ws, pipe.ws_bytes)
+    torch.cuda.synchronize()
+    for k in outs:
+        assert torch.equal(outs[k], res[k]), k
+
+
+def test_deterministic_repeats(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=512, D=256, H=128, E=8, K=4)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    first = None
+    for _ in range(3):
+        run_gpu(pipe, inp, (3, 5))
+        cur = [getattr(pipe, k).clone() for k in ("score", "sel_pos", "dw_gate", "dw_up",
+                                                   "dw_down", "dx")]
+        if first is None:
+            first = cur
+        else:
+            for a, b in zip(first, cur):
+                assert torch.equal(a, b)
+
+
+def test_bad_expert_ids_and_quotas_are_flagged(dev):
+    from demand_side_expert_gb300 import lrm
+    cfg = get_config("qwen3-30b-a3b-t4k", T=64, D=128, H=64, E=8, K=2)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    bad = inp["topk_idx"].clone()
+    bad[3, 1] = 99
+    bad[5, 0] = -4
+    pipe.dispatch(bad)
+    assert pipe.device_error() & lrm.LRM_DEVERR_EXPERT_ID
+    clamped = bad.clamp(0, cfg.E - 1).cpu().numpy()
+    check_dispatch(pipe, clamped, cfg.E)
+    pipe.clear_device_error()
+    pipe.dispatch(inp["topk_idx"])
+    quota = pipe.counts.clone()
+    quota[2] += 5
+    quota[4] = -1
+    ab = pipe.to_dispatch_order(inp["ab_pair"])
+    phi = pipe.to_dispatch_order(inp["phi_pair"])
+    pipe.quota.copy_(quota)
+    pipe.score_select_compact(inp["alpha"], inp["x"], inp["g"], ab, phi)
+    assert pipe.device_error() & lrm.LRM_DEVERR_QUOTA
+    q = to_np(pipe.quota).astype(np.int64)
+    n = to_np(pipe.counts).astype(np.int64)
+    assert np.array_equal(np.diff(to_np(pipe.sel_off)), np.clip(q, 0, n))
+
+
+# ---------------------------------------------------------------------------
+# full-size layers, in the launch configuration the benchmark times
+# ---------------------------------------------------------------------------
+def _full_size(name, rate, cap=0, sample_experts=3, sample_tokens=24, seed=None):
+    cfg = get_config(name)
+    dev = torch.device("cuda:0")
+    inp = generate(cfg, device=dev, seed=seed)
+    pipe = _pipe(cfg, dev)
+    run_gpu(pipe, inp, rate, cap)
+    assert pipe.device_error() == 0
+    nin = {k: (to_np(v) if torch.is_tensor(v) and k in ("topk_idx", "alpha") else v)
+           for k, v in inp.items()}
+    perm, inv, counts, off = check_dispatch(pipe, nin["topk_idx"], cfg.E)
+    qv = oracle.quota_from_rate(counts, rate[0], rate[1], cap)
+    assert np.array_equal(to_np(pipe.quota), qv)
+    N = cfg.N
+    rng = np.random.default_rng(0)
+    # scores on sampled positions, one by one
+    P = rng.choice(N, size=min(N, 4096), replace=False)
+    phi_s = to_np(pipe.to_dispatch_order(inp["phi_pair"])[torch.as_tensor(P, device=dev)])
+    ref = oracle.score(to_np(inp["g"]), phi_s, nin["alpha"], perm[P], cfg.K)
+    check_scores(to_np(pipe.score)[P], ref)
+    keep, sel_off, sel_pos = check_selection(pipe, perm, off, qv)
+    M = int(sel_off[-1])
+    assert np.array_equal(to_np(pipe.tok_c)[:M], perm[sel_pos] // cfg.K)
+    rop = np.full(N, -1)
+    rop[sel_pos] = np.arange(M)
+    assert np.array_equal(to_np(pipe.row_of_pos)[:N], rop)
+    # weight gradients of sampled experts (largest, smallest non-empty, random)
+    m = np.diff(sel_off)
+    nonempty = np.nonzero(m)[0]
+    picks = {int(np.argmax(m)), int(nonempty[np.argmin(m[nonempty])])}
+    picks |= set(int(e) for e in rng.choice(nonempty, size=sample_experts, replace=False))
+
+    def weights(e):
+        return tuple(to_np(inp[k][e:e + 1]) for k in ("w_gate", "w_up", "w_down"))
+
+    for e in sorted(picks):
+        lo, hi = int(sel_off[e]), int(sel_off[e + 1])
+        rows = slice(lo, hi)
+        b = oracle.expert_bwd(np.array([0, hi - lo]), *weights(e),
+                              to_np(pipe.dy_c[rows]), to_np(pipe.x_c[rows]),
+                              to_np(pipe.ab_c[rows]), to_np(pipe.phi_c[rows]))
+        for k in ("dw_gate", "dw_up", "dw_down"):
+            err = rel_fro(to_np(getattr(pipe, k)[e]), b[k][0])
+            assert err <= 2e-2, (name, e, k, err)
+    # dx on sampled tokens: sum of the oracle's rows for the kept slots
+    for t in rng.choice(cfg.T, size=sample_tokens, replace=False):
+        want = np.zeros(cfg.D)
+        for k in range(cfg.K):
+            j = int(rop[inv[t * cfg.K + k]])
+            if j < 0:
+                continue
+            e = int(np.searchsorted(sel_off, j, side="right") - 1)
+            _, dxc = oracle.expert_bwd_rows(np.array([0]), np.array([0, 1]), *weights(e),
+                                            to_np(pipe.dy_c[j:j + 1]),
+                                            to_np(pipe.ab_c[j:j + 1]))
+            want += dxc[0]
+        got = to_np(pipe.dx[int(t)])
+        assert np.linalg.norm(got - want) <= 2e-2 * max(np.linalg.norm(want), 1e-12), (name, t)
+    return pipe
+
+
+def test_full_size_qwen3_t4k(dev):
+    _full_size("qwen3-30b-a3b-t4k", (3, 5))
+
+
+def test_full_size_qwen3_t32k(dev):
+    pipe = _full_size("qwen3-30b-a3b-t32k", (1, 2))
+    counts = to_np(pipe.counts)
+    assert counts.max() > 10 * counts.mean()
+
+
+@pytest.mark.parametrize("rate", [(1, 4), (1, 1)])
+def test_full_size_glm45_sweep(dev, rate):
+    pipe = _full_size("glm45-106b-a12b-t16k", rate)
+    if rate == (1, 1):
+        N = pipe.N
+        assert torch.equal(pipe.sel_pos[:N].long(), torch.arange(N, device=dev))
+
+
+def test_full_size_stress(dev):
+    cfg = get_config("stress-e256")
+    pipe = _full_size("stress-e256", (1, 2), cap=cfg.cap)
+    q = to_np(pipe.quota)
+    assert q.max() == cfg.cap

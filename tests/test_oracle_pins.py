@@ -351,7 +351,7 @@ def test_sampled_rows_match_full_backward():
     out = _full_backward(L, 3, 5)
     rows = np.arange(0, out["sel_pos"].size, 3)
     dab, dxc = oracle.expert_bwd_rows(rows, out["sel_off"], L["wg"], L["wu"], L["wd"],
-                                      out["dy_c"], out["ab_c"])
+                                      out["dy_c"][rows], out["ab_c"][rows])
     np.testing.assert_allclose(dab, out["dab_c"][rows], rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(dxc, out["dx_c"][rows], rtol=1e-13, atol=1e-15)
 
