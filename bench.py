@@ -1,0 +1,531 @@
+#!/usr/bin/env python
+"""Benchmark of the recalibrated MoE expert backward on GB300.
+
+One step = one pass of the whole path over one synthetic MoE layer with its
+inputs resident in HBM: dispatch permutation, quota rule, LRM score,
+per-expert top-q selection, compaction, the four grouped expert-backward
+products and the dx scatter (12 kernel launches). The metric is retained
+rows per second, M / step time, with M = sum_e q_e the retained
+token-expert pairs. The L2 is flushed (a 256 MiB write) before every timed
+step, outside the step's CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+    python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer
+(no collective on the data path); value = rows of all ranks / max time.
+Rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "retained-pair expert-backward rows/s; grouped-GEMM % BF16 peak; select GB/s"
+DEFAULT_CONFIG = "qwen3-30b-a3b-t4k"
+FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 12
+SEGMENTS = ["dispatch", "quota", "score", "select", "compact", "fc2_dgrad", "fc2_wgrad",
+            "fc1_wgrad", "fc1_dgrad", "scatter_dx"]
+# kernels whose names the launch list shows for each segment
+KERNEL_NAMES = {
+    "dispatch": "dispatch_{hist,scan,scatter}_kernel", "quota": "quota_kernel",
+    "score": "score_kernel", "select": "select_kernel", "compact": "compact_kernel",
+    "fc2_dgrad": "grouped_gemm_kernel<0>", "fc2_wgrad": "grouped_gemm_kernel<1>",
+    "fc1_wgrad": "grouped_gemm_kernel<2>", "fc1_dgrad": "grouped_gemm_kernel<3>",
+    "scatter_dx": "dx_gather_kernel",
+}
+# source file of each segment's kernel (for the traffic record's freshness check)
+KERNEL_SOURCE = {
+    "dispatch": "dispatch.cu", "quota": "dispatch.cu", "score": "score.cu",
+    "select": "select.cu", "compact": "compact.cu", "fc2_dgrad": "gemm_tc.cu",
+    "fc2_wgrad": "gemm_tc.cu", "fc1_wgrad": "gemm_tc.cu", "fc1_dgrad": "gemm_tc.cu",
+    "scatter_dx": "compact.cu",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--rate", default=None, help="retention rate num/den (default: the "
+                    "workload's first rate)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes and flops per launch
+# ---------------------------------------------------------------------------
+def algorithmic(cfg, M: int) -> dict:
+    """Bytes (and flops) each segment must move at minimum, per launch."""
+    T, D, H, E, K = cfg.T, cfg.D, cfg.H, cfg.E, cfg.K
+    N = T * K
+    s = 2 if cfg.dtype == "bf16" else 4
+    W = E * D * H * s  # one expert weight tensor, all experts
+    return {
+        "dispatch": {"bytes": 4 * N + 8 * N + 8 * E},
+        "quota": {"bytes": 8 * E},
+        "score": {"bytes": T * D * s + N * H * s + 4 * N + 4 * N + 4 * N},
+        "select": {"bytes": 4 * N + N + 4 * M + 16 * E},
+        "compact": {"bytes": 2 * M * (2 * D + 3 * H) * s + 4 * M * 4 + 5 * N},
+        "fc2_dgrad": {"bytes": M * D * s + W + 2 * (M * 2 * H * s), "flops": 2 * M * D * H},
+        "fc2_wgrad": {"bytes": M * H * s + M * D * s + E * H * D * 4, "flops": 2 * M * D * H},
+        "fc1_wgrad": {"bytes": M * D * s + M * 2 * H * s + 2 * E * D * H * 4,
+                      "flops": 4 * M * D * H},
+        "fc1_dgrad": {"bytes": M * 2 * H * s + 2 * W + M * D * 4, "flops": 4 * M * D * H},
+        "scatter_dx": {"bytes": M * D * 4 + T * D * 4 + 8 * N},
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained",
+                                                      pk["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def source_sha(fname: str) -> str:
+    p = os.path.join(ROOT, "demand_side_expert_gb300", "csrc", fname)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def load_traffic(workload: str) -> dict:
+    """DRAM bytes per launch recorded from ncu, keyed by segment, fresh only."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return out
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            seg, wl, sha, nbytes = line.split()[:4]
+            if wl == workload and seg in KERNEL_SOURCE and sha == source_sha(KERNEL_SOURCE[seg]):
+                out[seg] = int(nbytes)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our path
+# ---------------------------------------------------------------------------
+def aggregate_ranks(time_s: float, rows: int, device, dist=None):
+    """(max time over ranks, rows summed over ranks); replicas, weak scaling."""
+    if dist is None:
+        return time_s, float(rows)
+    import torch
+
+    t = torch.tensor([time_s, float(rows)], dtype=torch.float64, device=device)
+    tmax = t.clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(tmax[0]), float(t[1])
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    from demand_side_expert_gb300 import RecalibratedExpertBackward
+    from workloads import generate, get_config
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    cfg = get_config(args.config)
+    rate = tuple(int(v) for v in args.rate.split("/")) if args.rate else cfg.rates[0]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = generate(cfg, device=dev, seed=cfg.seed + rank)
+    pipe = RecalibratedExpertBackward(cfg.T, cfg.D, cfg.H, cfg.E, cfg.K, cfg.dtype, dev)
+    # forward side, once: dispatch and the saved state in dispatch order
+    pipe.dispatch(inp["topk_idx"])
+    ab = pipe.to_dispatch_order(inp["ab_pair"])
+    phi = pipe.to_dispatch_order(inp["phi_pair"])
+    del inp["ab_pair"], inp["phi_pair"]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev):
+        ev[0].record(stream)
+        pipe.dispatch(inp["topk_idx"])
+        ev[1].record(stream)
+        pipe.quota_from_rate(rate[0], rate[1], cfg.cap)
+        ev[2].record(stream)
+        pipe.score_pairs(inp["alpha"], inp["g"], phi)
+        ev[3].record(stream)
+        pipe.select()
+        ev[4].record(stream)
+        pipe.compact(inp["alpha"], inp["x"], inp["g"], ab, phi)
+        ev[5].record(stream)
+        pipe.fc2_dgrad(inp["w_down"])
+        ev[6].record(stream)
+        pipe.fc2_wgrad()
+        ev[7].record(stream)
+        pipe.fc1_wgrad()
+        ev[8].record(stream)
+        pipe.fc1_dgrad(inp["w_gate"], inp["w_up"])
+        ev[9].record(stream)
+        pipe.scatter_dx()
+        ev[10].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(len(SEGMENTS) + 1)]
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1)
+        step(new_events())
+    torch.cuda.synchronize(dev)
+    if pipe.device_error() != 0:
+        raise RuntimeError(f"device error word {pipe.device_error()} after warm-up")
+    M = pipe.retained_rows
+
+    events = [new_events() for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(1)  # L2 flush outside the step's events
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+
+    seg_ms = {s: [] for s in SEGMENTS}
+    step_ms = []
+    for ev in events:
+        for j, s in enumerate(SEGMENTS):
+            seg_ms[s].append(ev[j].elapsed_time(ev[j + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+    total_s = sum(step_ms) / 1e3
+    if pipe.device_error() != 0:
+        raise RuntimeError(f"device error word {pipe.device_error()} after timing")
+
+    total_max, rows_sum = aggregate_ranks(total_s, M * args.steps, dev, dist)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(pipe, inp, ab, phi, rate, cfg, flush, stream, args)
+
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    alg = algorithmic(cfg, M)
+    traffic = load_traffic(cfg.name)
+    kernels = {}
+    for s in SEGMENTS:
+        ms = statistics.mean(seg_ms[s])
+        k = {"ms": round(ms, 4), "kernels": KERNEL_NAMES[s],
+             "gbs": round(alg[s]["bytes"] / (ms * 1e-3) / 1e9, 1)}
+        if "flops" in alg[s]:
+            k["tflops"] = round(alg[s]["flops"] / (ms * 1e-3) / 1e12, 1)
+        kernels[s] = k
+    dominant = max(SEGMENTS, key=lambda s: statistics.mean(seg_ms[s]))
+    dom_ms = statistics.mean(seg_ms[dominant])
+    a = alg[dominant]
+    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = a.get("flops", 0) / (peaks["bf16_tflops"] * 1e12)
+    if t_tc > t_hbm:
+        achieved = a["flops"] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        achieved = a["bytes"] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(achieved / roof["peak"], 4)
+    roof["traffic"] = traffic.get(dominant)
+    roof["kernel"] = KERNEL_NAMES[dominant]
+    roof["algorithmic_bytes"] = a["bytes"]
+    if "flops" in a:
+        roof["algorithmic_flops"] = a["flops"]
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst)" \
+        if peaks["source"] == "measured" else "fallback"
+
+    gemm = ["fc2_dgrad", "fc2_wgrad", "fc1_wgrad", "fc1_dgrad"]
+    gemm_ms = sum(statistics.mean(seg_ms[s]) for s in gemm)
+    gemm_flops = sum(alg[s]["flops"] for s in gemm)
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    sel_ms = statistics.mean(seg_ms["select"])
+
+    line = {
+        "metric": METRIC,
+        "value": round(rows_sum / total_max, 1),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_max * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded router, SwiGLU forward state and cotangents)",
+        "config": {
+            "workload": cfg.name, "T": cfg.T, "D": cfg.D, "H": cfg.H, "E": cfg.E, "K": cfg.K,
+            "rho": f"{rate[0]}/{rate[1]}", "quota_cap": cfg.cap, "routed_pairs": cfg.N,
+            "retained_rows": M, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
+            "inputs": "resident in HBM",
+        },
+        "grouped_gemm_pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
+        "grouped_gemm_tflops": round(gemm_tflops, 1),
+        "select_gbs": round(alg["select"]["bytes"] / (sel_ms * 1e-3) / 1e9, 1),
+        "kernels": kernels,
+        "roofline": roof,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+        "wall_s": round(wall, 4),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    return line, cfg, rate
+
+
+def run_e2e(pipe, inp, ab, phi, rate, cfg, flush, stream, args):
+    """Same metric with the step's inputs copied in from pinned host memory
+    and the results (dx and the weight gradients, the host offload of the
+    expert-gradient queue) copied back, inside the timed region."""
+    import torch
+
+    names = ("topk_idx", "alpha", "x", "g")
+    host_in = {k: inp[k].cpu().pin_memory() for k in names}
+    host_in["ab"] = ab.cpu().pin_memory()
+    host_in["phi"] = phi.cpu().pin_memory()
+    dev_in = dict((k, inp[k]) for k in names)
+    dev_in["ab"], dev_in["phi"] = ab, phi
+    outs = ("dx", "dw_gate", "dw_up", "dw_down")
+    host_out = {k: torch.empty(getattr(pipe, k).shape, dtype=torch.float32,
+                               pin_memory=True) for k in outs}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for k, h in host_in.items():
+            dev_in[k].copy_(h, non_blocking=True)
+        pipe.step(dev_in["topk_idx"], dev_in["alpha"], dev_in["x"], dev_in["g"], dev_in["ab"],
+                  dev_in["phi"], inp["w_gate"], inp["w_up"], inp["w_down"], rate=rate,
+                  cap=cfg.cap)
+        for k in outs:
+            host_out[k].copy_(getattr(pipe, k), non_blocking=True)
+
+    steps = max(1, min(args.steps, 10))
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) / 1e3
+    M = pipe.retained_rows
+    return {"value": round(M * steps / tot, 1), "unit": "rows/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "path": "pinned host -> HBM copies, the C-ABI calls, HBM -> pinned host copies "
+                    "of dx and dW, all on one stream"}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(cfg, rate, T_s: int, seed: int):
+    """The first T_s tokens of the workload, as float64/int64 host arrays."""
+    import numpy as np
+    import torch
+
+    from workloads import generate, get_config
+
+    small = get_config(cfg.name, T=T_s) if T_s < cfg.T else cfg
+    inp = generate(small, device="cuda" if torch.cuda.is_available() else "cpu", seed=seed)
+
+    def f64(t):
+        t = t.detach().cpu()
+        return (t.float() if t.dtype == torch.bfloat16 else t).numpy().astype(np.float64)
+
+    arrs = {k: f64(inp[k]) for k in ("alpha", "x", "g", "w_gate", "w_up", "w_down",
+                                      "ab_pair", "phi_pair")}
+    arrs["topk_idx"] = inp["topk_idx"].cpu().numpy().astype(np.int64)
+    return small, arrs
+
+
+def oracle_step(small, rate, a):
+    import oracle
+
+    out = oracle.recalibrated_backward(
+        a["topk_idx"], a["alpha"], a["x"], a["g"], a["ab_pair"], a["phi_pair"], a["w_gate"],
+        a["w_up"], a["w_down"], E=small.E, num=rate[0], den=rate[1], cap=small.cap)
+    return int(out["sel_off"][-1])
+
+
+def cpu_baseline(cfg, rate, T_s: int):
+    small, a = oracle_sample(cfg, rate, T_s, cfg.seed)
+    warm, aw = oracle_sample(cfg, rate, 16, cfg.seed + 1)
+    oracle_step(warm, rate, aw)  # BLAS thread pool start-up, outside the timing
+    t0 = time.perf_counter()
+    M = oracle_step(small, rate, a)
+    dt = time.perf_counter() - t0
+    whole = "the whole workload" if small.T == cfg.T else \
+        f"a {small.T}-token layer of {cfg.name}'s recipe (same D, H, E, K, rho)"
+    return {"value": round(M / dt, 2), "unit": "rows/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{whole}: whole path once, {M} retained rows in {dt:.1f} s; "
+                      f"float64 NumPy (BLAS threads on all host cores)"}
+
+
+def oracle_tokens(cfg, rate, seconds: float) -> int:
+    """Tokens whose oracle pass takes about ``seconds`` on the host: a fixed
+    ~1 s (weight-gradient buffers) plus 12*D*H float64 flops per retained row
+    at ~32 GFLOP/s."""
+    rows = max(seconds - 1.0, 0.5) * 3.2e10 / (12.0 * cfg.D * cfg.H)
+    tokens = int(rows / (cfg.K * rate[0] / rate[1] if rate[0] else cfg.K))
+    return max(16, min(cfg.T, tokens))
+
+
+def run_reference(args, rank: int):
+    from workloads import get_config
+
+    if rank != 0:
+        return None
+    cfg = get_config(args.config)
+    rate = tuple(int(v) for v in args.rate.split("/")) if args.rate else cfg.rates[0]
+    per_step = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    small, a = oracle_sample(cfg, rate, oracle_tokens(cfg, rate, per_step), cfg.seed)
+    for _ in range(max(args.warmup, 0)):
+        oracle_step(small, rate, a)
+    t0 = time.perf_counter()
+    M = 0
+    for _ in range(args.steps):
+        M += oracle_step(small, rate, a)
+    dt = time.perf_counter() - t0
+    value = round(M / dt, 2)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": cfg.T, "D": cfg.D, "H": cfg.H, "E": cfg.E,
+                   "K": cfg.K, "rho": f"{rate[0]}/{rate[1]}", "sampled_tokens": small.T},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"a {small.T}-token layer of {cfg.name}'s recipe per "
+                                   f"step (same D, H, E, K, rho)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if out is not None:
+        line, cfg, rate = out
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(cfg, rate, oracle_tokens(cfg, rate, 15.0))
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

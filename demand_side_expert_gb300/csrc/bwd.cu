@@ -1,35 +1,120 @@
-// lrm_expert_bwd_grouped: argument checks and the launch sequence of the
-// expert backward (four grouped products, then the scatter back to tokens).
+// Expert-backward entry points: the one-call lrm_expert_bwd_grouped and its
+// five sub-steps (the four grouped products of LRMoE Sec. 3.4 and the
+// scatter of input gradients back to tokens), with their argument checks.
 #include "common.cuh"
 #include "internal.h"
 
 using namespace lrm;
+
+namespace {
+
+lrm_status check_common(const lrm_shape* s, const void* ws, size_t ws_bytes,
+                        const int32_t* sel_off) {
+  lrm_status st = check_shape(s);
+  if (st != LRM_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
+  if (!sel_off) return LRM_ERR_INVALID_ARG;
+  return LRM_OK;
+}
+
+// Every listed pointer non-null (row buffers may be null only when N == 0)
+// and 16-byte aligned.
+lrm_status check_ptrs(const lrm_shape* s, std::initializer_list<const void*> always,
+                      std::initializer_list<const void*> rows) {
+  for (const void* p : always) {
+    if (!p) return LRM_ERR_INVALID_ARG;
+    if (!aligned16(p)) return LRM_ERR_UNSUPPORTED;
+  }
+  const bool has_rows = (int64_t)s->T * s->K > 0;
+  for (const void* p : rows) {
+    if (!p) {
+      if (has_rows) return LRM_ERR_INVALID_ARG;
+      continue;
+    }
+    if (!aligned16(p)) return LRM_ERR_UNSUPPORTED;
+  }
+  return LRM_OK;
+}
+
+lrm_status run_parts(const BwdArgs& a, unsigned parts) {
+  return a.s->dtype == LRM_BF16 ? launch_bwd_tc(a, parts) : launch_bwd_f32(a, parts);
+}
+
+}  // namespace
+
+extern "C" lrm_status lrm_expert_fc2_dgrad(const lrm_shape* s, const int32_t* sel_off,
+                                           const void* w_down, const void* dy_c,
+                                           const void* ab_c, void* dab_c, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  lrm_status st = check_common(s, ws, ws_bytes, sel_off);
+  if (st != LRM_OK) return st;
+  if ((st = check_ptrs(s, {w_down}, {dy_c, ab_c, dab_c})) != LRM_OK) return st;
+  BwdArgs a{s, sel_off, nullptr, nullptr, w_down, dy_c, nullptr, ab_c, nullptr, dab_c,
+            nullptr, nullptr, nullptr, nullptr, error_word(ws), (cudaStream_t)stream};
+  return run_parts(a, kPartFc2Dgrad);
+}
+
+extern "C" lrm_status lrm_expert_fc2_wgrad(const lrm_shape* s, const int32_t* sel_off,
+                                           const void* phi_c, const void* dy_c, float* dw_down,
+                                           void* ws, size_t ws_bytes, void* stream) {
+  lrm_status st = check_common(s, ws, ws_bytes, sel_off);
+  if (st != LRM_OK) return st;
+  if ((st = check_ptrs(s, {dw_down}, {phi_c, dy_c})) != LRM_OK) return st;
+  BwdArgs a{s, sel_off, nullptr, nullptr, nullptr, dy_c, nullptr, nullptr, phi_c, nullptr,
+            nullptr, nullptr, nullptr, dw_down, error_word(ws), (cudaStream_t)stream};
+  return run_parts(a, kPartFc2Wgrad);
+}
+
+extern "C" lrm_status lrm_expert_fc1_wgrad(const lrm_shape* s, const int32_t* sel_off,
+                                           const void* x_c, const void* dab_c, float* dw_gate,
+                                           float* dw_up, void* ws, size_t ws_bytes,
+                                           void* stream) {
+  lrm_status st = check_common(s, ws, ws_bytes, sel_off);
+  if (st != LRM_OK) return st;
+  if ((st = check_ptrs(s, {dw_gate, dw_up}, {x_c, dab_c})) != LRM_OK) return st;
+  BwdArgs a{s, sel_off, nullptr, nullptr, nullptr, nullptr, x_c, nullptr, nullptr,
+            const_cast<void*>(dab_c), nullptr, dw_gate, dw_up, nullptr, error_word(ws),
+            (cudaStream_t)stream};
+  return run_parts(a, kPartFc1Wgrad);
+}
+
+extern "C" lrm_status lrm_expert_fc1_dgrad(const lrm_shape* s, const int32_t* sel_off,
+                                           const void* w_gate, const void* w_up,
+                                           const void* dab_c, float* dx_c, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  lrm_status st = check_common(s, ws, ws_bytes, sel_off);
+  if (st != LRM_OK) return st;
+  if ((st = check_ptrs(s, {w_gate, w_up}, {dab_c, dx_c})) != LRM_OK) return st;
+  BwdArgs a{s, sel_off, w_gate, w_up, nullptr, nullptr, nullptr, nullptr, nullptr,
+            const_cast<void*>(dab_c), dx_c, nullptr, nullptr, nullptr, error_word(ws),
+            (cudaStream_t)stream};
+  return run_parts(a, kPartFc1Dgrad);
+}
+
+extern "C" lrm_status lrm_scatter_dx(const lrm_shape* s, const float* dx_c, const int32_t* inv,
+                                     const int32_t* row_of_pos, float* dx, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  lrm_status st = check_shape(s);
+  if (st != LRM_OK) return st;
+  if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
+  if (s->K > 32) return LRM_ERR_UNSUPPORTED;
+  if ((st = check_ptrs(s, {}, {dx_c, inv, row_of_pos, dx})) != LRM_OK) return st;
+  return launch_dx_gather(s, dx_c, inv, row_of_pos, dx, error_word(ws), (cudaStream_t)stream);
+}
 
 extern "C" lrm_status lrm_expert_bwd_grouped(
     const lrm_shape* s, const int32_t* sel_off, const void* w_gate, const void* w_up,
     const void* w_down, const void* dy_c, const void* x_c, const void* ab_c, const void* phi_c,
     const int32_t* inv, const int32_t* row_of_pos, void* dab_c, float* dx_c, float* dw_gate,
     float* dw_up, float* dw_down, float* dx, void* ws, size_t ws_bytes, void* stream) {
-  lrm_status st = check_shape(s);
+  lrm_status st = check_common(s, ws, ws_bytes, sel_off);
   if (st != LRM_OK) return st;
-  if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
   if (s->K > 32) return LRM_ERR_UNSUPPORTED;
-  const void* ptrs[] = {sel_off, w_gate, w_up, w_down, dw_gate, dw_up, dw_down};
-  for (const void* p : ptrs)
-    if (!p) return LRM_ERR_INVALID_ARG;
-  const int64_t N = (int64_t)s->T * s->K;
-  if (N > 0) {
-    const void* rows[] = {dy_c, x_c, ab_c, phi_c, inv, row_of_pos, dab_c, dx_c, dx};
-    for (const void* p : rows)
-      if (!p) return LRM_ERR_INVALID_ARG;
-  }
-  const void* vec[] = {w_gate, w_up, w_down, dy_c, x_c, ab_c, phi_c, dab_c, dx_c,
-                       dw_gate, dw_up, dw_down, dx};
-  for (const void* p : vec)
-    if (p && !aligned16(p)) return LRM_ERR_UNSUPPORTED;
+  if ((st = check_ptrs(s, {w_gate, w_up, w_down, dw_gate, dw_up, dw_down},
+                       {dy_c, x_c, ab_c, phi_c, inv, row_of_pos, dab_c, dx_c, dx})) != LRM_OK)
+    return st;
   BwdArgs a{s, sel_off, w_gate, w_up, w_down, dy_c, x_c, ab_c, phi_c, dab_c,
             dx_c, dw_gate, dw_up, dw_down, error_word(ws), (cudaStream_t)stream};
-  st = s->dtype == LRM_BF16 ? launch_bwd_tc(a) : launch_bwd_f32(a);
-  if (st != LRM_OK) return st;
+  if ((st = run_parts(a, kPartAll)) != LRM_OK) return st;
   return launch_dx_gather(s, dx_c, inv, row_of_pos, dx, error_word(ws), (cudaStream_t)stream);
 }

@@ -95,7 +95,7 @@ __global__ void f32_g3_kernel(const int32_t* __restrict__ sel_off, int E, int D,
   }
 }
 
-lrm_status launch_bwd_f32(const BwdArgs& a) {
+lrm_status launch_bwd_f32(const BwdArgs& a, unsigned parts) {
   const lrm_shape* s = a.s;
   const int D = s->D, H = s->H, E = s->E;
   const int64_t N = (int64_t)s->T * s->K;
@@ -106,17 +106,21 @@ lrm_status launch_bwd_f32(const BwdArgs& a) {
   };
   cudaStream_t cs = a.stream;
   const float* dy = (const float*)a.dy_c;
-  f32_g1_kernel<<<grid(N * H), kF32Threads, 0, cs>>>(a.sel_off, E, D, H, dy,
-                                                     (const float*)a.w_down,
-                                                     (const float*)a.ab_c, (float*)a.dab_c);
-  f32_g2_kernel<<<grid((int64_t)E * H * D), kF32Threads, 0, cs>>>(
-      a.sel_off, E, D, H, (const float*)a.phi_c, dy, a.dw_down);
-  f32_g3_kernel<<<grid((int64_t)E * D * 2 * H), kF32Threads, 0, cs>>>(
-      a.sel_off, E, D, H, (const float*)a.x_c, (const float*)a.dab_c, a.dw_gate, a.dw_up);
-  f32_g4_kernel<<<grid(N * D), kF32Threads, 0, cs>>>(a.sel_off, E, D, H,
-                                                     (const float*)a.dab_c,
-                                                     (const float*)a.w_gate,
-                                                     (const float*)a.w_up, a.dx_c);
+  if (parts & kPartFc2Dgrad)
+    f32_g1_kernel<<<grid(N * H), kF32Threads, 0, cs>>>(a.sel_off, E, D, H, dy,
+                                                       (const float*)a.w_down,
+                                                       (const float*)a.ab_c, (float*)a.dab_c);
+  if (parts & kPartFc2Wgrad)
+    f32_g2_kernel<<<grid((int64_t)E * H * D), kF32Threads, 0, cs>>>(
+        a.sel_off, E, D, H, (const float*)a.phi_c, dy, a.dw_down);
+  if (parts & kPartFc1Wgrad)
+    f32_g3_kernel<<<grid((int64_t)E * D * 2 * H), kF32Threads, 0, cs>>>(
+        a.sel_off, E, D, H, (const float*)a.x_c, (const float*)a.dab_c, a.dw_gate, a.dw_up);
+  if (parts & kPartFc1Dgrad)
+    f32_g4_kernel<<<grid(N * D), kF32Threads, 0, cs>>>(a.sel_off, E, D, H,
+                                                       (const float*)a.dab_c,
+                                                       (const float*)a.w_gate,
+                                                       (const float*)a.w_up, a.dx_c);
   return launch_status();
 }
 

@@ -694,27 +694,13 @@ static lrm_status launch_mode(const CUtensorMap& a, const CUtensorMap& b, const 
 
 }  // namespace tc
 
-lrm_status launch_bwd_tc(const BwdArgs& a) {
+lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   using namespace tc;
   const lrm_shape* s = a.s;
   const int D = s->D, H = s->H, E = s->E;
   if (D % 64 != 0 || H % 64 != 0) return LRM_ERR_UNSUPPORTED;
   const uint64_t N = (uint64_t)s->T * s->K;
   const uint64_t rows = std::max<uint64_t>(N, 1);
-  CUtensorMap m_dy_k, m_dab_k, m_wdown, m_wgate, m_wup, m_phi_mn, m_dy_mn, m_x_mn, m_dab_mn;
-  bool ok = true;
-  // K-major operands of the data-gradient products
-  ok &= make_map(&m_dy_k, a.dy_c, 2, 1, rows, D, 64, BM);
-  ok &= make_map(&m_dab_k, a.dab_c, 2, 1, rows, 2 * H, 64, BM);
-  ok &= make_map(&m_wdown, a.w_down, 3, E, H, D, 64, BN);
-  ok &= make_map(&m_wgate, a.w_gate, 3, E, D, H, 64, BN);
-  ok &= make_map(&m_wup, a.w_up, 3, E, D, H, 64, BN);
-  // MN-major operands of the weight-gradient products (64 x 64 boxes)
-  ok &= make_map(&m_phi_mn, a.phi_c, 2, 1, rows, H, 64, 64);
-  ok &= make_map(&m_dy_mn, a.dy_c, 2, 1, rows, D, 64, 64);
-  ok &= make_map(&m_x_mn, a.x_c, 2, 1, rows, D, 64, 64);
-  ok &= make_map(&m_dab_mn, a.dab_c, 2, 1, rows, 2 * H, 64, 64);
-  if (!ok) return LRM_ERR_CUDA;
 
   Params p;
   p.E = E;
@@ -724,29 +710,60 @@ lrm_status launch_bwd_tc(const BwdArgs& a) {
   p.sel_off = a.sel_off;
   p.ab_c = reinterpret_cast<const __nv_bfloat16*>(a.ab_c);
   p.dab_c = reinterpret_cast<__nv_bfloat16*>(a.dab_c);
-  p.err = a.err;
-  const int sms = num_sms();
-  const int64_t dg_tiles_n1 = ((int64_t)N / BM + E) * ((H + BN - 1) / BN);
-  const int64_t dg_tiles_n4 = ((int64_t)N / BM + E) * ((D + BN - 1) / BN);
-  const int64_t wg2 = (int64_t)E * ((H + BM - 1) / BM) * ((D + BN - 1) / BN);
-  const int64_t wg3 = (int64_t)E * ((D + BM - 1) / BM) * ((2 * H + BN - 1) / BN);
-  auto grid_of = [&](int64_t tiles) { return (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sms)); };
-
-  lrm_status st;
   p.out0 = nullptr;
   p.out1 = nullptr;
-  if ((st = launch_mode<kG1>(m_dy_k, m_wdown, m_wdown, p, grid_of(dg_tiles_n1), a.stream)) != LRM_OK)
-    return st;
-  p.out0 = a.dw_down;
-  if ((st = launch_mode<kG2>(m_phi_mn, m_dy_mn, m_dy_mn, p, grid_of(wg2), a.stream)) != LRM_OK)
-    return st;
-  p.out0 = a.dw_gate;
-  p.out1 = a.dw_up;
-  if ((st = launch_mode<kG3>(m_x_mn, m_dab_mn, m_dab_mn, p, grid_of(wg3), a.stream)) != LRM_OK)
-    return st;
-  p.out0 = a.dx_c;
-  p.out1 = nullptr;
-  return launch_mode<kG4>(m_dab_k, m_wgate, m_wup, p, grid_of(dg_tiles_n4), a.stream);
+  p.err = a.err;
+  const int sms = num_sms();
+  auto grid_of = [&](int64_t tiles) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
+  };
+  lrm_status st = LRM_OK;
+  // K-major operands (data-gradient products): boxes of 64 x BM rows (A) and
+  // 64 x BN rows (weights, one expert per 3-D slice); MN-major operands
+  // (weight-gradient products): 64 x 64 boxes.
+  if (parts & kPartFc2Dgrad) {
+    CUtensorMap m_dy, m_wdown;
+    if (!make_map(&m_dy, a.dy_c, 2, 1, rows, D, 64, BM) ||
+        !make_map(&m_wdown, a.w_down, 3, E, H, D, 64, BN))
+      return LRM_ERR_CUDA;
+    const int64_t tiles = ((int64_t)N / BM + E) * ((H + BN - 1) / BN);
+    if ((st = launch_mode<kG1>(m_dy, m_wdown, m_wdown, p, grid_of(tiles), a.stream)) != LRM_OK)
+      return st;
+  }
+  if (parts & kPartFc2Wgrad) {
+    CUtensorMap m_phi, m_dy;
+    if (!make_map(&m_phi, a.phi_c, 2, 1, rows, H, 64, 64) ||
+        !make_map(&m_dy, a.dy_c, 2, 1, rows, D, 64, 64))
+      return LRM_ERR_CUDA;
+    p.out0 = a.dw_down;
+    const int64_t tiles = (int64_t)E * ((H + BM - 1) / BM) * ((D + BN - 1) / BN);
+    if ((st = launch_mode<kG2>(m_phi, m_dy, m_dy, p, grid_of(tiles), a.stream)) != LRM_OK)
+      return st;
+  }
+  if (parts & kPartFc1Wgrad) {
+    CUtensorMap m_x, m_dab;
+    if (!make_map(&m_x, a.x_c, 2, 1, rows, D, 64, 64) ||
+        !make_map(&m_dab, a.dab_c, 2, 1, rows, 2 * H, 64, 64))
+      return LRM_ERR_CUDA;
+    p.out0 = a.dw_gate;
+    p.out1 = a.dw_up;
+    const int64_t tiles = (int64_t)E * ((D + BM - 1) / BM) * ((2 * H + BN - 1) / BN);
+    if ((st = launch_mode<kG3>(m_x, m_dab, m_dab, p, grid_of(tiles), a.stream)) != LRM_OK)
+      return st;
+  }
+  if (parts & kPartFc1Dgrad) {
+    CUtensorMap m_dab, m_wgate, m_wup;
+    if (!make_map(&m_dab, a.dab_c, 2, 1, rows, 2 * H, 64, BM) ||
+        !make_map(&m_wgate, a.w_gate, 3, E, D, H, 64, BN) ||
+        !make_map(&m_wup, a.w_up, 3, E, D, H, 64, BN))
+      return LRM_ERR_CUDA;
+    p.out0 = a.dx_c;
+    p.out1 = nullptr;
+    const int64_t tiles = ((int64_t)N / BM + E) * ((D + BN - 1) / BN);
+    if ((st = launch_mode<kG4>(m_dab, m_wgate, m_wup, p, grid_of(tiles), a.stream)) != LRM_OK)
+      return st;
+  }
+  return st;
 }
 
 }  // namespace lrm

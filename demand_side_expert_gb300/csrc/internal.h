@@ -18,10 +18,19 @@ struct BwdArgs {
   cudaStream_t stream;
 };
 
-// BF16 path: four persistent tcgen05 grouped GEMMs (tensor cores).
-lrm_status launch_bwd_tc(const BwdArgs& a);
-// F32 path: the same four products on CUDA cores.
-lrm_status launch_bwd_f32(const BwdArgs& a);
+// Sub-steps of the expert backward, in dependency order.
+enum : unsigned {
+  kPartFc2Dgrad = 1,  // dphi = dy_c W_down^T + SwiGLU gradient -> dab_c
+  kPartFc2Wgrad = 2,  // dW_down = phi_c^T dy_c
+  kPartFc1Wgrad = 4,  // [dW_gate | dW_up] = x_c^T dab_c
+  kPartFc1Dgrad = 8,  // dx_c = dab_c [W_gate | W_up]^T
+  kPartAll = 15
+};
+
+// BF16 path: persistent tcgen05 grouped GEMMs (tensor cores).
+lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts);
+// F32 path: the same products on CUDA cores.
+lrm_status launch_bwd_f32(const BwdArgs& a, unsigned parts);
 // dx[t] = sum over kept slots of dx_c rows (deterministic, no atomics).
 lrm_status launch_dx_gather(const lrm_shape* s, const float* dx_c, const int32_t* inv,
                             const int32_t* row_of_pos, float* dx, int32_t* err,

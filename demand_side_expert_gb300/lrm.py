@@ -23,7 +23,8 @@ EXPORTS = (
     "lrm_workspace_bytes", "lrm_clear_device_error", "lrm_get_device_error",
     "lrm_status_string", "lrm_dispatch_permute", "lrm_permute_rows",
     "lrm_quota_from_rate", "lrm_score", "lrm_select_quota", "lrm_compact",
-    "lrm_expert_bwd_grouped",
+    "lrm_expert_bwd_grouped", "lrm_expert_fc2_dgrad", "lrm_expert_fc2_wgrad",
+    "lrm_expert_fc1_wgrad", "lrm_expert_fc1_dgrad", "lrm_scatter_dx",
 )
 
 
@@ -58,6 +59,11 @@ def _load():
         "lrm_select_quota": (i32, [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_compact": (i32, [sp] + [vp] * 15 + [vp, sz, vp]),
         "lrm_expert_bwd_grouped": (i32, [sp] + [vp] * 16 + [vp, sz, vp]),
+        "lrm_expert_fc2_dgrad": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_expert_fc2_wgrad": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_expert_fc1_wgrad": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_expert_fc1_dgrad": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_scatter_dx": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -167,3 +173,33 @@ def lrm_expert_bwd_grouped(shape, sel_off, w_gate, w_up, w_down, dy_c, x_c, ab_c
         ctypes.byref(shape), _p(sel_off), _p(w_gate), _p(w_up), _p(w_down), _p(dy_c), _p(x_c),
         _p(ab_c), _p(phi_c), _p(inv), _p(row_of_pos), _p(dab_c), _p(dx_c), _p(dw_gate),
         _p(dw_up), _p(dw_down), _p(dx), _p(ws), ws_bytes, _s(stream)))
+
+
+def lrm_expert_fc2_dgrad(shape, sel_off, w_down, dy_c, ab_c, dab_c, ws, ws_bytes, stream=None):
+    _check("lrm_expert_fc2_dgrad", _lib.lrm_expert_fc2_dgrad(
+        ctypes.byref(shape), _p(sel_off), _p(w_down), _p(dy_c), _p(ab_c), _p(dab_c), _p(ws),
+        ws_bytes, _s(stream)))
+
+
+def lrm_expert_fc2_wgrad(shape, sel_off, phi_c, dy_c, dw_down, ws, ws_bytes, stream=None):
+    _check("lrm_expert_fc2_wgrad", _lib.lrm_expert_fc2_wgrad(
+        ctypes.byref(shape), _p(sel_off), _p(phi_c), _p(dy_c), _p(dw_down), _p(ws), ws_bytes,
+        _s(stream)))
+
+
+def lrm_expert_fc1_wgrad(shape, sel_off, x_c, dab_c, dw_gate, dw_up, ws, ws_bytes, stream=None):
+    _check("lrm_expert_fc1_wgrad", _lib.lrm_expert_fc1_wgrad(
+        ctypes.byref(shape), _p(sel_off), _p(x_c), _p(dab_c), _p(dw_gate), _p(dw_up), _p(ws),
+        ws_bytes, _s(stream)))
+
+
+def lrm_expert_fc1_dgrad(shape, sel_off, w_gate, w_up, dab_c, dx_c, ws, ws_bytes, stream=None):
+    _check("lrm_expert_fc1_dgrad", _lib.lrm_expert_fc1_dgrad(
+        ctypes.byref(shape), _p(sel_off), _p(w_gate), _p(w_up), _p(dab_c), _p(dx_c), _p(ws),
+        ws_bytes, _s(stream)))
+
+
+def lrm_scatter_dx(shape, dx_c, inv, row_of_pos, dx, ws, ws_bytes, stream=None):
+    _check("lrm_scatter_dx", _lib.lrm_scatter_dx(
+        ctypes.byref(shape), _p(dx_c), _p(inv), _p(row_of_pos), _p(dx), _p(ws), ws_bytes,
+        _s(stream)))

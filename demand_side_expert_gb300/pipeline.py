@@ -7,8 +7,8 @@ calls of liblrm in order on one CUDA stream:
   lrm_dispatch_permute -> lrm_quota_from_rate -> lrm_score ->
   lrm_select_quota -> lrm_compact -> lrm_expert_bwd_grouped
 
-Every step of the path runs in liblrm's kernels; this class only allocates,
-passes pointers and copies host buffers in and out (``run_host``).
+Every step of the path runs in liblrm's kernels; this class only allocates
+and passes pointers.
 """
 
 from __future__ import annotations
@@ -37,7 +37,7 @@ class RecalibratedExpertBackward:
         dev = torch.device(device)
         self.device = dev
         i32, f32, dt = torch.int32, torch.float32, self.tdtype
-        N, rows = self.N, max(self.N, 1)
+        rows = max(self.N, 1)
 
         def empty(*shape, dtype):
             return torch.empty(*shape, dtype=dtype, device=dev)
@@ -60,7 +60,6 @@ class RecalibratedExpertBackward:
         self.dw_down = empty(E, H, D, dtype=f32)
         self.dx = empty(max(T, 1), D, dtype=f32)
         lrm.lrm_clear_device_error(self.ws, self.ws_bytes)
-        del N
 
     # -- forward side -------------------------------------------------------
     def dispatch(self, topk_idx, stream=None):
@@ -78,20 +77,51 @@ class RecalibratedExpertBackward:
     def quota_from_rate(self, num: int, den: int, cap: int = 0, stream=None):
         lrm.lrm_quota_from_rate(self.counts, self.E, num, den, cap, self.quota, stream)
 
+    def score_pairs(self, alpha, g, phi, stream=None):
+        lrm.lrm_score(self.shape, g, phi, alpha, self.inv, self.score, self.ws, self.ws_bytes,
+                      stream)
+
+    def select(self, stream=None):
+        lrm.lrm_select_quota(self.shape, self.score, self.off, self.quota, self.keep,
+                             self.sel_off, self.sel_pos, self.ws, self.ws_bytes, stream)
+
+    def compact(self, alpha, x, g, ab, phi, stream=None):
+        lrm.lrm_compact(self.shape, self.perm, self.keep, self.sel_off, self.sel_pos, alpha, x,
+                        g, ab, phi, self.dy_c, self.x_c, self.ab_c, self.phi_c, self.tok_c,
+                        self.row_of_pos, self.ws, self.ws_bytes, stream)
+
     def score_select_compact(self, alpha, x, g, ab, phi, stream=None):
-        s, w, wb = self.shape, self.ws, self.ws_bytes
-        lrm.lrm_score(s, g, phi, alpha, self.inv, self.score, w, wb, stream)
-        lrm.lrm_select_quota(s, self.score, self.off, self.quota, self.keep, self.sel_off,
-                             self.sel_pos, w, wb, stream)
-        lrm.lrm_compact(s, self.perm, self.keep, self.sel_off, self.sel_pos, alpha, x, g, ab,
-                        phi, self.dy_c, self.x_c, self.ab_c, self.phi_c, self.tok_c,
-                        self.row_of_pos, w, wb, stream)
+        self.score_pairs(alpha, g, phi, stream)
+        self.select(stream)
+        self.compact(alpha, x, g, ab, phi, stream)
 
     def expert_bwd(self, w_gate, w_up, w_down, stream=None):
         lrm.lrm_expert_bwd_grouped(
             self.shape, self.sel_off, w_gate, w_up, w_down, self.dy_c, self.x_c, self.ab_c,
             self.phi_c, self.inv, self.row_of_pos, self.dab_c, self.dx_c, self.dw_gate,
             self.dw_up, self.dw_down, self.dx, self.ws, self.ws_bytes, stream)
+
+    # the same backward as five separate calls (one kernel each), so that a
+    # caller can time or overlap the sub-steps
+    def fc2_dgrad(self, w_down, stream=None):
+        lrm.lrm_expert_fc2_dgrad(self.shape, self.sel_off, w_down, self.dy_c, self.ab_c,
+                                 self.dab_c, self.ws, self.ws_bytes, stream)
+
+    def fc2_wgrad(self, stream=None):
+        lrm.lrm_expert_fc2_wgrad(self.shape, self.sel_off, self.phi_c, self.dy_c, self.dw_down,
+                                 self.ws, self.ws_bytes, stream)
+
+    def fc1_wgrad(self, stream=None):
+        lrm.lrm_expert_fc1_wgrad(self.shape, self.sel_off, self.x_c, self.dab_c, self.dw_gate,
+                                 self.dw_up, self.ws, self.ws_bytes, stream)
+
+    def fc1_dgrad(self, w_gate, w_up, stream=None):
+        lrm.lrm_expert_fc1_dgrad(self.shape, self.sel_off, w_gate, w_up, self.dab_c, self.dx_c,
+                                 self.ws, self.ws_bytes, stream)
+
+    def scatter_dx(self, stream=None):
+        lrm.lrm_scatter_dx(self.shape, self.dx_c, self.inv, self.row_of_pos, self.dx, self.ws,
+                           self.ws_bytes, stream)
 
     def step(self, topk_idx, alpha, x, g, ab, phi, w_gate, w_up, w_down, rate=(1, 1),
              cap: int = 0, quota: torch.Tensor | None = None, stream=None):

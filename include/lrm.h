@@ -215,6 +215,38 @@ lrm_status lrm_expert_bwd_grouped(const lrm_shape* shape, const int32_t* sel_off
                                   float* dw_down, float* dx, void* ws,
                                   size_t ws_bytes, void* stream);
 
+/*
+ * The five sub-steps of lrm_expert_bwd_grouped as separate calls, same
+ * arithmetic, arguments and layouts as documented there (LRMoE Sec. 3.4:
+ * "the FC1 and FC2 data-gradient and weight-gradient operations" over the
+ * retained rows). Issue them in this order on one stream; each reads only
+ * what the earlier ones wrote.
+ *   lrm_expert_fc2_dgrad : dab_c = SwiGLU-grad(dy_c W_down[e]^T, ab_c)
+ *   lrm_expert_fc2_wgrad : dW_down[e] = phi_c^T dy_c        (overwritten)
+ *   lrm_expert_fc1_wgrad : dW_gate[e], dW_up[e] = x_c^T dab_c (overwritten)
+ *   lrm_expert_fc1_dgrad : dx_c = dab_c [W_gate | W_up][e]^T
+ *   lrm_scatter_dx       : dx[t] = sum of the token's kept dx_c rows
+ */
+lrm_status lrm_expert_fc2_dgrad(const lrm_shape* shape, const int32_t* sel_off,
+                                const void* w_down, const void* dy_c,
+                                const void* ab_c, void* dab_c, void* ws,
+                                size_t ws_bytes, void* stream);
+lrm_status lrm_expert_fc2_wgrad(const lrm_shape* shape, const int32_t* sel_off,
+                                const void* phi_c, const void* dy_c,
+                                float* dw_down, void* ws, size_t ws_bytes,
+                                void* stream);
+lrm_status lrm_expert_fc1_wgrad(const lrm_shape* shape, const int32_t* sel_off,
+                                const void* x_c, const void* dab_c,
+                                float* dw_gate, float* dw_up, void* ws,
+                                size_t ws_bytes, void* stream);
+lrm_status lrm_expert_fc1_dgrad(const lrm_shape* shape, const int32_t* sel_off,
+                                const void* w_gate, const void* w_up,
+                                const void* dab_c, float* dx_c, void* ws,
+                                size_t ws_bytes, void* stream);
+lrm_status lrm_scatter_dx(const lrm_shape* shape, const float* dx_c,
+                          const int32_t* inv, const int32_t* row_of_pos,
+                          float* dx, void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ HEADER = os.path.join(ROOT, "include", "lrm.h")
 def _declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(lrm_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(lrm_[a-z0-9_]+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")

@@ -295,3 +295,26 @@ def test_full_size_stress(dev):
     pipe = _full_size("stress-e256", (1, 2), cap=cfg.cap)
     q = to_np(pipe.quota)
     assert q.max() == cfg.cap
+
+
+def test_split_substeps_match_one_call(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=512, D=256, H=192, E=8, K=4)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    run_gpu(pipe, inp, (1, 2))
+    ref = {k: getattr(pipe, k).clone() for k in ("dab_c", "dx_c", "dw_gate", "dw_up",
+                                                  "dw_down", "dx")}
+    for k in ref:
+        getattr(pipe, k).fill_(float("nan"))
+    pipe.fc2_dgrad(inp["w_down"])
+    pipe.fc2_wgrad()
+    pipe.fc1_wgrad()
+    pipe.fc1_dgrad(inp["w_gate"], inp["w_up"])
+    pipe.scatter_dx()
+    torch.cuda.synchronize()
+    M = pipe.retained_rows
+    for k, v in ref.items():
+        got = getattr(pipe, k)
+        if k in ("dab_c", "dx_c"):
+            got, v = got[:M], v[:M]
+        assert torch.equal(got, v), k
