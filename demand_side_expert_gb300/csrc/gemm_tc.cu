@@ -19,8 +19,11 @@
 //             tcgen05.mma (M=128, N=256, K=16) into one of two 256-column
 //             accumulators; tcgen05.commit frees smem stages and hands
 //             finished accumulators to the epilogue;
-//   warps 2-5 epilogue: tcgen05.ld rows out of TMEM (one row per thread),
-//             fused SwiGLU gradient (G1) or masked FP32 stores.
+//   warps 2-5 epilogue: tcgen05.ld rows out of TMEM (one row per thread);
+//             G1 fuses the SwiGLU gradient (saved a, b rows prefetched one
+//             32-column chunk ahead); FP32 outputs go through a per-warp
+//             32x32 swizzled shared-memory block and a TMA bulk-tensor store,
+//             so every 128-byte line is written whole.
 // Data-gradient tiles are cut at group ends (rows past m_e are computed and
 // masked on store). Weight-gradient tiles reduce over [sel_off[e],
 // sel_off[e+1]) in 64-row blocks; rows of the last block that belong to the
@@ -46,14 +49,22 @@ constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t BOX_BYTES = 64 * 64 * 2;  // one 64x64 MN-major box
 constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t STAGING_BYTES = 32 * 32 * 4;  // one 32x32 fp32 block, 128B-swizzled
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
 enum Mode { kG1 = 0, kG2 = 1, kG3 = 2, kG4 = 3 };
 
+// Operand maps (A, B, second B for G4) and output maps (G2: dW_down,
+// G3: dW_gate and dW_up, G4: dx_c), passed by value in parameter space.
+struct Maps {
+  CUtensorMap a, b, b2, o1, o2;
+};
+
 struct Params {
   int E, D, H;
-  int n_rows;  // row capacity of the compacted buffers
+  int n_rows;      // row capacity of the compacted buffers
+  int stage_bufs;  // 32x32 fp32 staging blocks per epilogue warp (0, 1 or 2)
   const int32_t* sel_off;
   const __nv_bfloat16* ab_c;
   __nv_bfloat16* dab_c;
@@ -156,6 +167,36 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(su32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
       : "memory");
+}
+// TMA bulk-tensor stores (shared -> global), completion tracked per bulk group
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
+                                             int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(su32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x,
+                                             int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(su32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until at most `pending` committed bulk groups may still read shared memory
+__device__ __forceinline__ void bulk_wait_read(int pending) {
+  if (pending > 0)
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  else
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -289,7 +330,7 @@ __device__ __forceinline__ Tile decode(const Sched& s, int tau) {
 }
 
 // ----------------------------------------------------------------------------
-// epilogues (one thread = one accumulator row, 32 columns per call)
+// epilogues (one thread = one accumulator row, 32 columns per chunk)
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&r)[32]) {
   float4* d = reinterpret_cast<float4*>(dst);
@@ -298,25 +339,25 @@ __device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&r)[32]
     d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                        __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
 }
-__device__ __forceinline__ void zero_f32x32(float* dst) {
-  float4* d = reinterpret_cast<float4*>(dst);
+
+// Row `lane` of a 32x32 fp32 block into the 128B-swizzled layout a TMA store
+// with a 32 x 32 box expects: 16-byte chunk j of row r sits at chunk j^(r%8).
+__device__ __forceinline__ void stage_row(uint8_t* blk, int lane, const uint32_t (&r)[32]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) d[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint4*>(blk + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
 }
 
-// SwiGLU gradient of 32 columns h..h+31 of compacted row j.
-__device__ __forceinline__ void swiglu_epilogue(const Params& p, int64_t j, int h,
-                                                const uint32_t (&r)[32]) {
-  const int H = p.H;
-  const uint4* arow = reinterpret_cast<const uint4*>(p.ab_c + j * 2 * H + h);
-  const uint4* brow = reinterpret_cast<const uint4*>(p.ab_c + j * 2 * H + H + h);
-  uint4* darow = reinterpret_cast<uint4*>(p.dab_c + j * 2 * H + h);
-  uint4* dbrow = reinterpret_cast<uint4*>(p.dab_c + j * 2 * H + H + h);
+// SwiGLU gradient of 32 columns, given the row's a and b values.
+__device__ __forceinline__ void swiglu_chunk(const uint32_t (&r)[32], const uint4 (&av)[4],
+                                             const uint4 (&bv)[4], uint4 (&dav)[4],
+                                             uint4 (&dbv)[4]) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     float a[8], b[8], da[8], db[8];
-    Vec16<__nv_bfloat16>::unpack(arow[v], a);
-    Vec16<__nv_bfloat16>::unpack(brow[v], b);
+    Vec16<__nv_bfloat16>::unpack(av[v], a);
+    Vec16<__nv_bfloat16>::unpack(bv[v], b);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const float dphi = __uint_as_float(r[8 * v + u]);
@@ -324,30 +365,9 @@ __device__ __forceinline__ void swiglu_epilogue(const Params& p, int64_t j, int 
       da[u] = dphi * b[u] * s * (1.0f + a[u] * (1.0f - s));
       db[u] = dphi * a[u] * s;
     }
-    darow[v] = Vec16<__nv_bfloat16>::pack(da);
-    dbrow[v] = Vec16<__nv_bfloat16>::pack(db);
+    dav[v] = Vec16<__nv_bfloat16>::pack(da);
+    dbv[v] = Vec16<__nv_bfloat16>::pack(db);
   }
-}
-
-// Output location of 32 consecutive accumulator columns (row, col); nullptr
-// when the chunk is outside the output (masked).
-template <int MODE>
-__device__ __forceinline__ float* out_ptr(const Params& p, const Tile& t, int row_local,
-                                          int col) {
-  if constexpr (MODE == kG4) {
-    if (row_local >= t.valid || col >= p.D) return nullptr;
-    return p.out0 + (int64_t)(t.m0 + row_local) * p.D + col;
-  } else if constexpr (MODE == kG2) {
-    const int h = t.m0 + row_local;
-    if (h >= p.H || col >= p.D) return nullptr;
-    return p.out0 + ((int64_t)t.e * p.H + h) * p.D + col;
-  } else if constexpr (MODE == kG3) {
-    const int d = t.m0 + row_local;
-    if (d >= p.D || col >= 2 * p.H) return nullptr;
-    if (col < p.H) return p.out0 + ((int64_t)t.e * p.D + d) * p.H + col;
-    return p.out1 + ((int64_t)t.e * p.D + d) * p.H + (col - p.H);
-  }
-  return nullptr;
 }
 
 // ----------------------------------------------------------------------------
@@ -355,15 +375,15 @@ __device__ __forceinline__ float* out_ptr(const Params& p, const Tile& t, int ro
 // ----------------------------------------------------------------------------
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
-                    const __grid_constant__ CUtensorMap mapB,
-                    const __grid_constant__ CUtensorMap mapB2, const Params p) {
+grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr bool WG = Geo<MODE>::kWgrad;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // 4 warps x stage_bufs blocks
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(staging + 4 * p.stage_bufs * STAGING_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -374,6 +394,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
   int* goff = bad_flag + 1;          // [E+1]
   int* tab = goff + p.E + 1;         // dgrad: tpre[E+1]; wgrad: order[E]
+  const CUtensorMap* mapA = &maps.a;
+  const CUtensorMap* mapB = &maps.b;
+  const CUtensorMap* mapB2 = &maps.b2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E;
@@ -384,12 +407,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     *bad_flag = 0;
   }
   __syncthreads();
-  const int nrows_cap = p.n_rows;
   for (int i = tid; i <= E; i += kThreads) {
     const int v = p.sel_off[i];
     const int prev = i > 0 ? p.sel_off[i - 1] : 0;
     goff[i] = v;
-    if (v < prev || (i == 0 && v != 0) || v > nrows_cap) *bad_flag = 1;
+    if (v < prev || (i == 0 && v != 0) || v > p.n_rows) *bad_flag = 1;
   }
   __syncthreads();
   if (*bad_flag) {
@@ -459,9 +481,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
-    prefetch_map(&mapA);
-    prefetch_map(&mapB);
-    if (MODE == kG4) prefetch_map(&mapB2);
+    prefetch_map(mapA);
+    prefetch_map(mapB);
+    if (MODE == kG4) prefetch_map(mapB2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -490,23 +512,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           uint8_t* b_s = a_s + A_BYTES;
           mbar_expect_tx(&full[stage], STAGE_BYTES);
           if constexpr (MODE == kG1) {
-            tma_load_2d(a_s, &mapA, &full[stage], kb * BK, t.m0);
-            tma_load_3d(b_s, &mapB, &full[stage], kb * BK, t.n0, t.e);
+            tma_load_2d(a_s, mapA, &full[stage], kb * BK, t.m0);
+            tma_load_3d(b_s, mapB, &full[stage], kb * BK, t.n0, t.e);
           } else if constexpr (MODE == kG4) {
-            tma_load_2d(a_s, &mapA, &full[stage], kb * BK, t.m0);
+            tma_load_2d(a_s, mapA, &full[stage], kb * BK, t.m0);
             const int hb = p.H / BK;
             if (kb < hb)
-              tma_load_3d(b_s, &mapB, &full[stage], kb * BK, t.n0, t.e);
+              tma_load_3d(b_s, mapB, &full[stage], kb * BK, t.n0, t.e);
             else
-              tma_load_3d(b_s, &mapB2, &full[stage], (kb - hb) * BK, t.n0, t.e);
+              tma_load_3d(b_s, mapB2, &full[stage], (kb - hb) * BK, t.n0, t.e);
           } else {
             const int y = t.row0 + kb * BK;
 #pragma unroll
             for (int i = 0; i < BM / 64; ++i)
-              tma_load_2d(a_s + i * BOX_BYTES, &mapA, &full[stage], t.m0 + 64 * i, y);
+              tma_load_2d(a_s + i * BOX_BYTES, mapA, &full[stage], t.m0 + 64 * i, y);
 #pragma unroll
             for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(b_s + i * BOX_BYTES, &mapB, &full[stage], t.n0 + 64 * i, y);
+              tma_load_2d(b_s + i * BOX_BYTES, mapB, &full[stage], t.n0 + 64 * i, y);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -553,7 +575,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
               uint8_t* box = bx < BM / 64 ? a_s + bx * BOX_BYTES : b_s + (bx - BM / 64) * BOX_BYTES;
               *reinterpret_cast<uint4*>(box + (valid + rz) * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            fence_async_smem();
             __syncwarp();
           }
         }
@@ -599,14 +621,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     // ===================== epilogue (warps 2..5) =====================
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_local = q * 32 + lane;
+    const int nbuf = p.stage_bufs;
+    uint8_t* wst = staging + (warp - 2) * nbuf * STAGING_BYTES;
+    int buf = 0;
+    const int ncols = MODE == kG3 ? 2 * p.H : p.D;  // output width (G2, G3, G4)
+    const int row_lim = MODE == kG2 ? p.H : p.D;    // output rows (G2, G3)
     uint32_t acc = 0, acc_phase = 0;
+
+    // stage 32 accumulator columns of this warp's 32 rows and store them
+    auto staged_store = [&](const uint32_t (&r)[32], const Tile& t, int col) {
+      if (lane == 0) bulk_wait_read(nbuf - 1);
+      __syncwarp();
+      uint8_t* blk = wst + buf * STAGING_BYTES;
+      stage_row(blk, lane, r);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (MODE == kG2) {
+          tma_store_3d(&maps.o1, blk, col, t.m0 + q * 32, t.e);
+        } else if constexpr (MODE == kG3) {
+          if (col < p.H)
+            tma_store_3d(&maps.o1, blk, col, t.m0 + q * 32, t.e);
+          else
+            tma_store_3d(&maps.o2, blk, col - p.H, t.m0 + q * 32, t.e);
+        } else {
+          tma_store_2d(&maps.o1, blk, col, t.m0 + q * 32);
+        }
+        bulk_commit();
+      }
+      if (nbuf == 2) buf ^= 1;
+    };
+
     for (int tau = blockIdx.x; tau < sc.total; tau += gridDim.x) {
       const Tile t = decode<MODE>(sc, tau);
-      if (t.nkb <= 0) {  // expert without retained rows: zero weight gradient
+      if (t.nkb <= 0) {
+        // expert without retained rows: its weight gradient is zero
         if constexpr (WG) {
-          for (int c = 0; c < BN; c += 32) {
-            float* dst = out_ptr<MODE>(p, t, row_local, t.n0 + c);
-            if (dst) zero_f32x32(dst);
+          if (t.m0 + q * 32 < row_lim) {
+            if (lane == 0) bulk_wait_read(0);
+            __syncwarp();
+            uint32_t z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+            buf = 0;
+            for (int c = 0; c < BN; c += 32)
+              if (t.n0 + c < ncols) staged_store(z, t, t.n0 + c);
           }
         }
         continue;
@@ -614,17 +673,61 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c, r);
-        tmem_ld_wait();
-        if constexpr (MODE == kG1) {
+      if constexpr (MODE == kG1) {
+        const bool rv = row_local < t.valid;
+        const int64_t j = (int64_t)t.m0 + row_local;
+        const __nv_bfloat16* arow = p.ab_c + j * 2 * p.H;
+        __nv_bfloat16* drow = p.dab_c + j * 2 * p.H;
+        uint4 a_cur[4], b_cur[4], a_nxt[4], b_nxt[4];
+        auto load_ab = [&](int h, uint4 (&av)[4], uint4 (&bv)[4]) {
+          if (rv && h < p.H) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              av[v] = ld_stream(arow + h + 8 * v);
+              bv[v] = ld_stream(arow + p.H + h + 8 * v);
+            }
+          }
+        };
+        load_ab(t.n0, a_cur, b_cur);
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          if (c + 32 < BN) load_ab(t.n0 + c + 32, a_nxt, b_nxt);
+          tmem_ld_wait();
           const int h = t.n0 + c;
-          if (row_local < t.valid && h < p.H) swiglu_epilogue(p, (int64_t)t.m0 + row_local, h, r);
-        } else {
-          float* dst = out_ptr<MODE>(p, t, row_local, t.n0 + c);
-          if (dst) store_f32x32(dst, r);
+          if (rv && h < p.H) {
+            uint4 dav[4], dbv[4];
+            swiglu_chunk(r, a_cur, b_cur, dav, dbv);
+            uint4* da_dst = reinterpret_cast<uint4*>(drow + h);
+            uint4* db_dst = reinterpret_cast<uint4*>(drow + p.H + h);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              da_dst[v] = dav[v];
+              db_dst[v] = dbv[v];
+            }
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            a_cur[v] = a_nxt[v];
+            b_cur[v] = b_nxt[v];
+          }
+        }
+      } else {
+        const bool rows_in = WG ? (t.m0 + q * 32 < row_lim) : (q * 32 < t.valid);
+        const bool whole = WG || (q * 32 + 32 <= t.valid);  // G4: block inside the group
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          tmem_ld_wait();
+          const int col = t.n0 + c;
+          if (!rows_in || col >= ncols) continue;
+          if (whole) {
+            staged_store(r, t, col);
+          } else if (row_local < t.valid) {  // G4 block crossing the group end
+            store_f32x32(p.out0 + (int64_t)(t.m0 + row_local) * p.D + col, r);
+          }
         }
       }
       tc_fence_before();
@@ -632,6 +735,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_all();  // staged stores done before smem goes away
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -661,34 +766,40 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 row-major [rows, cols] (rank 2) or [E, rows, cols] (rank 3), 128B swizzle.
-static bool make_map(CUtensorMap* m, const void* base, int rank, uint64_t E, uint64_t rows,
-                     uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+// Row-major [rows, cols] (rank 2) or [E, rows, cols] (rank 3) map with a
+// 128-byte swizzle; bf16 operands or fp32 outputs.
+static bool make_map(CUtensorMap* m, const void* base, bool fp32, int rank, uint64_t E,
+                     uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const uint64_t es = fp32 ? 4 : 2;
   cuuint64_t dims[3] = {cols, rows, E};
-  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint64_t strides[2] = {cols * es, rows * cols * es};
   cuuint32_t box[3] = {box_cols, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static size_t smem_bytes(int E) {
-  return 1024 + STAGES * STAGE_BYTES + 128 + 16 + (size_t)(2 * (E + 1) + 2) * 4;
+constexpr size_t kSmemLimit = 232448;  // 227 KB per block
+
+static size_t smem_bytes(int E, int stage_bufs) {
+  return 1024 + STAGES * STAGE_BYTES + (size_t)4 * stage_bufs * STAGING_BYTES + 128 + 16 +
+         (size_t)(2 * (E + 1) + 2) * 4;
 }
 
 template <int MODE>
-static lrm_status launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
-                              const Params& p, int grid, cudaStream_t cs) {
-  const size_t smem = smem_bytes(p.E);
+static lrm_status launch_mode(const Maps& maps, Params p, int grid, cudaStream_t cs) {
+  p.stage_bufs = MODE == kG1 ? 0 : (smem_bytes(p.E, 2) <= kSmemLimit ? 2 : 1);
+  const size_t smem = smem_bytes(p.E, p.stage_bufs);
+  if (smem > kSmemLimit) return LRM_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return LRM_ERR_CUDA;
-  grouped_gemm_kernel<MODE><<<grid, kThreads, smem, cs>>>(a, b, b2, p);
+  grouped_gemm_kernel<MODE><<<grid, kThreads, smem, cs>>>(maps, p);
   return launch_status();
 }
 
@@ -707,6 +818,7 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   p.D = D;
   p.H = H;
   p.n_rows = (int)N;
+  p.stage_bufs = 0;
   p.sel_off = a.sel_off;
   p.ab_c = reinterpret_cast<const __nv_bfloat16*>(a.ab_c);
   p.dab_c = reinterpret_cast<__nv_bfloat16*>(a.dab_c);
@@ -720,48 +832,53 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   lrm_status st = LRM_OK;
   // K-major operands (data-gradient products): boxes of 64 x BM rows (A) and
   // 64 x BN rows (weights, one expert per 3-D slice); MN-major operands
-  // (weight-gradient products): 64 x 64 boxes.
+  // (weight-gradient products): 64 x 64 boxes; fp32 outputs: 32 x 32 boxes.
   if (parts & kPartFc2Dgrad) {
-    CUtensorMap m_dy, m_wdown;
-    if (!make_map(&m_dy, a.dy_c, 2, 1, rows, D, 64, BM) ||
-        !make_map(&m_wdown, a.w_down, 3, E, H, D, 64, BN))
+    Maps m;
+    if (!make_map(&m.a, a.dy_c, false, 2, 1, rows, D, 64, BM) ||
+        !make_map(&m.b, a.w_down, false, 3, E, H, D, 64, BN))
       return LRM_ERR_CUDA;
+    m.b2 = m.o1 = m.o2 = m.b;
     const int64_t tiles = ((int64_t)N / BM + E) * ((H + BN - 1) / BN);
-    if ((st = launch_mode<kG1>(m_dy, m_wdown, m_wdown, p, grid_of(tiles), a.stream)) != LRM_OK)
-      return st;
+    if ((st = launch_mode<kG1>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
   }
   if (parts & kPartFc2Wgrad) {
-    CUtensorMap m_phi, m_dy;
-    if (!make_map(&m_phi, a.phi_c, 2, 1, rows, H, 64, 64) ||
-        !make_map(&m_dy, a.dy_c, 2, 1, rows, D, 64, 64))
+    Maps m;
+    if (!make_map(&m.a, a.phi_c, false, 2, 1, rows, H, 64, 64) ||
+        !make_map(&m.b, a.dy_c, false, 2, 1, rows, D, 64, 64) ||
+        !make_map(&m.o1, a.dw_down, true, 3, E, H, D, 32, 32))
       return LRM_ERR_CUDA;
+    m.b2 = m.b;
+    m.o2 = m.o1;
     p.out0 = a.dw_down;
     const int64_t tiles = (int64_t)E * ((H + BM - 1) / BM) * ((D + BN - 1) / BN);
-    if ((st = launch_mode<kG2>(m_phi, m_dy, m_dy, p, grid_of(tiles), a.stream)) != LRM_OK)
-      return st;
+    if ((st = launch_mode<kG2>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
   }
   if (parts & kPartFc1Wgrad) {
-    CUtensorMap m_x, m_dab;
-    if (!make_map(&m_x, a.x_c, 2, 1, rows, D, 64, 64) ||
-        !make_map(&m_dab, a.dab_c, 2, 1, rows, 2 * H, 64, 64))
+    Maps m;
+    if (!make_map(&m.a, a.x_c, false, 2, 1, rows, D, 64, 64) ||
+        !make_map(&m.b, a.dab_c, false, 2, 1, rows, 2 * H, 64, 64) ||
+        !make_map(&m.o1, a.dw_gate, true, 3, E, D, H, 32, 32) ||
+        !make_map(&m.o2, a.dw_up, true, 3, E, D, H, 32, 32))
       return LRM_ERR_CUDA;
+    m.b2 = m.b;
     p.out0 = a.dw_gate;
     p.out1 = a.dw_up;
     const int64_t tiles = (int64_t)E * ((D + BM - 1) / BM) * ((2 * H + BN - 1) / BN);
-    if ((st = launch_mode<kG3>(m_x, m_dab, m_dab, p, grid_of(tiles), a.stream)) != LRM_OK)
-      return st;
+    if ((st = launch_mode<kG3>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
   }
   if (parts & kPartFc1Dgrad) {
-    CUtensorMap m_dab, m_wgate, m_wup;
-    if (!make_map(&m_dab, a.dab_c, 2, 1, rows, 2 * H, 64, BM) ||
-        !make_map(&m_wgate, a.w_gate, 3, E, D, H, 64, BN) ||
-        !make_map(&m_wup, a.w_up, 3, E, D, H, 64, BN))
+    Maps m;
+    if (!make_map(&m.a, a.dab_c, false, 2, 1, rows, 2 * H, 64, BM) ||
+        !make_map(&m.b, a.w_gate, false, 3, E, D, H, 64, BN) ||
+        !make_map(&m.b2, a.w_up, false, 3, E, D, H, 64, BN) ||
+        !make_map(&m.o1, a.dx_c, true, 2, 1, rows, D, 32, 32))
       return LRM_ERR_CUDA;
+    m.o2 = m.o1;
     p.out0 = a.dx_c;
     p.out1 = nullptr;
     const int64_t tiles = ((int64_t)N / BM + E) * ((D + BN - 1) / BN);
-    if ((st = launch_mode<kG4>(m_dab, m_wgate, m_wup, p, grid_of(tiles), a.stream)) != LRM_OK)
-      return st;
+    if ((st = launch_mode<kG4>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
   }
   return st;
 }
