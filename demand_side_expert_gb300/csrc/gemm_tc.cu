@@ -19,7 +19,8 @@
 //             tcgen05.mma (M=128, N=256, K=16) into one of two 256-column
 //             accumulators; tcgen05.commit frees smem stages and hands
 //             finished accumulators to the epilogue;
-//   warps 2-5 epilogue: tcgen05.ld rows out of TMEM (one row per thread);
+//   warps 2-9 epilogue: tcgen05.ld rows out of TMEM (one row per thread,
+//             two warps per 32-lane quarter, each half of the columns);
 //             G1 fuses the SwiGLU gradient (saved a, b rows prefetched one
 //             32-column chunk ahead); FP32 outputs go through a per-warp
 //             32x32 swizzled shared-memory block and a TMA bulk-tensor store,
@@ -42,8 +43,10 @@
 namespace lrm {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int kThreads = 192;
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int MAX_STAGES = 4;  // smem ring depth; 3 when the staging blocks need room
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -65,6 +68,7 @@ struct Params {
   int E, D, H;
   int n_rows;      // row capacity of the compacted buffers
   int stage_bufs;  // 32x32 fp32 staging blocks per epilogue warp (0, 1 or 2)
+  int stages;      // depth of the operand ring (3 or 4)
   const int32_t* sel_off;
   const __nv_bfloat16* ab_c;
   __nv_bfloat16* dab_c;
@@ -361,7 +365,7 @@ __device__ __forceinline__ void swiglu_chunk(const uint32_t (&r)[32], const uint
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const float dphi = __uint_as_float(r[8 * v + u]);
-      const float s = 1.0f / (1.0f + __expf(-a[u]));
+      const float s = __fdividef(1.0f, 1.0f + __expf(-a[u]));
       da[u] = dphi * b[u] * s * (1.0f + a[u] * (1.0f - s));
       db[u] = dphi * a[u] * s;
     }
@@ -381,12 +385,13 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // 4 warps x stage_bufs blocks
+  const int STAGES = p.stages;
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // kEpiWarps x stage_bufs blocks
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(staging + 4 * p.stage_bufs * STAGING_BYTES);
+      reinterpret_cast<uint64_t*>(staging + kEpiWarps * p.stage_bufs * STAGING_BYTES);
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* empty = bars + MAX_STAGES;
+  uint64_t* tfull = bars + 2 * MAX_STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -475,7 +480,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -539,7 +544,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
       }
       // every issued copy must land before the CTA may exit
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < MAX_STAGES; ++s)
         if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_parity >> s) & 1u);
     }
   } else if (warp == 1) {
@@ -618,9 +623,10 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     }
     __syncwarp();
   } else {
-    // ===================== epilogue (warps 2..5) =====================
+    // ===================== epilogue (warps 2..9) =====================
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_local = q * 32 + lane;
+    const int c_lo = ((warp - 2) >> 2) * (BN / 2), c_hi = c_lo + BN / 2;  // its columns
     const int nbuf = p.stage_bufs;
     uint8_t* wst = staging + (warp - 2) * nbuf * STAGING_BYTES;
     int buf = 0;
@@ -664,7 +670,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0u;
             buf = 0;
-            for (int c = 0; c < BN; c += 32)
+            for (int c = c_lo; c < c_hi; c += 32)
               if (t.n0 + c < ncols) staged_store(z, t, t.n0 + c);
           }
         }
@@ -688,12 +694,12 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             }
           }
         };
-        load_ab(t.n0, a_cur, b_cur);
+        load_ab(t.n0 + c_lo, a_cur, b_cur);
 #pragma unroll
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + c, r);
-          if (c + 32 < BN) load_ab(t.n0 + c + 32, a_nxt, b_nxt);
+          if (c + 32 < c_hi) load_ab(t.n0 + c + 32, a_nxt, b_nxt);
           tmem_ld_wait();
           const int h = t.n0 + c;
           if (rv && h < p.H) {
@@ -717,7 +723,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const bool rows_in = WG ? (t.m0 + q * 32 < row_lim) : (q * 32 < t.valid);
         const bool whole = WG || (q * 32 + 32 <= t.valid);  // G4: block inside the group
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + c, r);
           tmem_ld_wait();
@@ -785,15 +791,17 @@ static bool make_map(CUtensorMap* m, const void* base, bool fp32, int rank, uint
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
 
-static size_t smem_bytes(int E, int stage_bufs) {
-  return 1024 + STAGES * STAGE_BYTES + (size_t)4 * stage_bufs * STAGING_BYTES + 128 + 16 +
+static size_t smem_bytes(int E, int stages, int stage_bufs) {
+  return 1024 + (size_t)stages * STAGE_BYTES + (size_t)kEpiWarps * stage_bufs * STAGING_BYTES +
+         128 + 16 +
          (size_t)(2 * (E + 1) + 2) * 4;
 }
 
 template <int MODE>
 static lrm_status launch_mode(const Maps& maps, Params p, int grid, cudaStream_t cs) {
-  p.stage_bufs = MODE == kG1 ? 0 : (smem_bytes(p.E, 2) <= kSmemLimit ? 2 : 1);
-  const size_t smem = smem_bytes(p.E, p.stage_bufs);
+  p.stage_bufs = MODE == kG1 ? 0 : 1;
+  p.stages = smem_bytes(p.E, MAX_STAGES, p.stage_bufs) <= kSmemLimit ? MAX_STAGES : 3;
+  const size_t smem = smem_bytes(p.E, p.stages, p.stage_bufs);
   if (smem > kSmemLimit) return LRM_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -819,6 +827,7 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   p.H = H;
   p.n_rows = (int)N;
   p.stage_bufs = 0;
+  p.stages = MAX_STAGES;
   p.sel_off = a.sel_off;
   p.ab_c = reinterpret_cast<const __nv_bfloat16*>(a.ab_c);
   p.dab_c = reinterpret_cast<__nv_bfloat16*>(a.dab_c);
