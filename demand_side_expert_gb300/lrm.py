@@ -25,7 +25,9 @@ EXPORTS = (
     "lrm_quota_from_rate", "lrm_score", "lrm_select_quota", "lrm_compact",
     "lrm_expert_bwd_grouped", "lrm_expert_fc2_dgrad", "lrm_expert_fc2_wgrad",
     "lrm_expert_fc1_wgrad", "lrm_expert_fc1_dgrad", "lrm_scatter_dx",
+    "lrm_dispatch_permute_noalloc",
 )
+LRM_NOALLOC_MAX_CHUNK_ENTRIES = 65536
 
 
 class LrmError(RuntimeError):
@@ -64,6 +66,7 @@ def _load():
         "lrm_expert_fc1_wgrad": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_expert_fc1_dgrad": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_scatter_dx": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_dispatch_permute_noalloc": (i32, [sp, vp, vp, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -203,3 +206,15 @@ def lrm_scatter_dx(shape, dx_c, inv, row_of_pos, dx, ws, ws_bytes, stream=None):
     _check("lrm_scatter_dx", _lib.lrm_scatter_dx(
         ctypes.byref(shape), _p(dx_c), _p(inv), _p(row_of_pos), _p(dx), _p(ws), ws_bytes,
         _s(stream)))
+
+
+def lrm_dispatch_permute_noalloc(shape, topk_idx, perm, inv, counts, off, dev_err=None,
+                                 stream=None):
+    """Dispatch permutation that allocates nothing (scratch built into the library).
+
+    For callers that may not allocate device memory; see include/lrm.h for
+    the size limit and the rule that overlapping calls race.
+    """
+    _check("lrm_dispatch_permute_noalloc", _lib.lrm_dispatch_permute_noalloc(
+        ctypes.byref(shape), _p(topk_idx), _p(perm), _p(inv), _p(counts), _p(off),
+        _p(dev_err), _s(stream)))

@@ -216,6 +216,36 @@ lrm_status lrm_expert_bwd_grouped(const lrm_shape* shape, const int32_t* sel_off
                                   size_t ws_bytes, void* stream);
 
 /*
+ * lrm_dispatch_permute for callers that cannot allocate device memory (the
+ * paper has no counterpart; this is a deployment variant). Some callers are
+ * handed only their input and output tensors, e.g. a plugin inside a host
+ * whose memory manager owns the whole device budget; a cudaMalloc there
+ * would bypass that accounting and can stall the whole device. This entry
+ * point allocates nothing: its per-chunk tables live in one file-scope
+ * device array of 2 * LRM_NOALLOC_MAX_CHUNK_ENTRIES int32 (512 KiB), which
+ * every GPU that loads the library holds until the process exits.
+ *  - Same outputs as lrm_dispatch_permute (bit for bit). dev_err may be
+ *    NULL; otherwise LRM_DEVERR_EXPERT_ID is ORed into *dev_err (a 4-byte
+ *    device word the caller clears).
+ *  - Limit: E * ceil(T*K / 2048) <= LRM_NOALLOC_MAX_CHUNK_ENTRIES, else
+ *    LRM_ERR_WORKSPACE is returned before anything is launched (the built-in
+ *    scratch is too small; use lrm_dispatch_permute with a workspace).
+ *  - The first call on each device looks up the array's device address with
+ *    cudaGetSymbolAddress (once, with that device current); make that first
+ *    call before any stream capture.
+ *  - All calls share the one array: calls whose kernels overlap on the GPU
+ *    (different streams, or several host threads) race and corrupt each
+ *    other's results; serialise them. Every table entry a call reads is
+ *    written earlier in the same call, so stale contents are harmless.
+ */
+#define LRM_NOALLOC_MAX_CHUNK_ENTRIES 65536
+lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* shape,
+                                        const int32_t* topk_idx, int32_t* perm,
+                                        int32_t* inv, int32_t* counts,
+                                        int32_t* off, int32_t* dev_err,
+                                        void* stream);
+
+/*
  * The five sub-steps of lrm_expert_bwd_grouped as separate calls, same
  * arithmetic, arguments and layouts as documented there (LRMoE Sec. 3.4:
  * "the FC1 and FC2 data-gradient and weight-gradient operations" over the
