@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--rate", default=None, help="retention rate num/den (default: the "
                     "workload's first rate)")
+    ap.add_argument("--override", default="",
+                    help="comma-separated shape overrides of the workload, e.g. T=2048,E=16 "
+                    "(a scaled variant; the workload name records them)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -196,17 +199,31 @@ def aggregate_ranks(time_s: float, rows: int, device, dist=None):
     return float(tmax[0]), float(t[1])
 
 
+def workload_of(args):
+    from workloads import get_config
+
+    over = {}
+    for item in filter(None, args.override.split(",")):
+        k, v = item.split("=")
+        over[k.strip()] = int(v)
+    cfg = get_config(args.config, **over)
+    if over:
+        tag = ",".join(f"{k}={v}" for k, v in sorted(over.items()))
+        cfg = type(cfg)(**{**cfg.__dict__, "name": f"{cfg.name}[{tag}]"})
+    return cfg
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
 
     from demand_side_expert_gb300 import RecalibratedExpertBackward
-    from workloads import generate, get_config
+    from workloads import generate
 
     dist = None
     if world > 1:
         import torch.distributed as dist
 
-    cfg = get_config(args.config)
+    cfg = workload_of(args)
     rate = tuple(int(v) for v in args.rate.split("/")) if args.rate else cfg.rates[0]
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -417,9 +434,9 @@ def oracle_sample(cfg, rate, T_s: int, seed: int):
     import numpy as np
     import torch
 
-    from workloads import generate, get_config
+    from workloads import generate, with_tokens
 
-    small = get_config(cfg.name, T=T_s) if T_s < cfg.T else cfg
+    small = with_tokens(cfg, T_s) if T_s < cfg.T else cfg
     inp = generate(small, device="cuda" if torch.cuda.is_available() else "cpu", seed=seed)
 
     def f64(t):
@@ -466,11 +483,9 @@ def oracle_tokens(cfg, rate, seconds: float) -> int:
 
 
 def run_reference(args, rank: int):
-    from workloads import get_config
-
     if rank != 0:
         return None
-    cfg = get_config(args.config)
+    cfg = workload_of(args)
     rate = tuple(int(v) for v in args.rate.split("/")) if args.rate else cfg.rates[0]
     per_step = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
     small, a = oracle_sample(cfg, rate, oracle_tokens(cfg, rate, per_step), cfg.seed)

@@ -34,12 +34,14 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link liblrm.so; returns its path. Raises on failure."""
+def build(verbose: bool = False, ptxas_info: bool = False, extra: list | None = None) -> str:
+    """Compile and link liblrm.so; returns its path. Raises on failure.
+
+    ``extra``: additional nvcc flags (e.g. a -D to build a variant)."""
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = list(extra or []) + (["-Xptxas", "-v"] if ptxas_info else [])
 
     def compile_one(src: str):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")

@@ -43,13 +43,18 @@
 namespace lrm {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int MAX_STAGES = 4;  // smem ring depth; 3 when the staging blocks need room
+constexpr int BM = 128, BN = 256, BK = 64;  // rows per CTA, accumulator columns, K block
+constexpr int MAX_STAGES = 6;  // operand ring depth (runtime: as deep as shared memory allows)
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+// B rows a CTA loads: all BN columns alone, half of them in a CTA pair
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr uint32_t kStageBytes = A_BYTES + kBRows * BK * 2;  // 32 or 48 KB
+  static constexpr int kTileRows = PAIR ? 2 * BM : BM;                // M of one MMA
+};
 constexpr uint32_t BOX_BYTES = 64 * 64 * 2;  // one 64x64 MN-major box
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t STAGING_BYTES = 32 * 32 * 4;  // one 32x32 fp32 block, 128B-swizzled
@@ -206,6 +211,80 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---- CTA pairs (cluster of 2) ----
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory location in CTA `rank`
+__device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(su32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// arrive on a barrier of another CTA of the cluster (release at CTA scope)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// the same without ordering: for arrivals whose data is tracked by tx bytes
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
+}
+// TMA load whose completion is counted on a barrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t mbar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t mbar_cluster, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   su32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the barrier at the same offset in every CTA of `mask` once this
+// thread's earlier pair MMAs have completed
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(su32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    su32(slot)),
@@ -288,33 +367,36 @@ struct Geo {
 // ----------------------------------------------------------------------------
 struct Tile {
   int e;       // expert
-  int m0;      // dgrad: first compacted row; wgrad: first output row
+  int m0;      // dgrad: first compacted row of the unit's tile; wgrad: first output row
   int n0;      // first output column
   int nkb;     // 64-wide K blocks
-  int valid;   // dgrad: rows of the tile inside the group; wgrad: rows of the last K block
+  int valid;   // dgrad: rows of the unit's tile inside the group; wgrad: rows of the last K block
   int row0;    // wgrad: first compacted row of the group
+  int cm0;     // this CTA's first row (m0 + rank * 128)
+  int cvalid;  // dgrad: this CTA's rows inside the group (may be <= 0)
 };
 
 struct Sched {
   const int* goff;   // [E+1] group offsets (validated copy of sel_off)
   const int* tpre;   // dgrad: [E+1] tile prefix
   const int* order;  // wgrad: experts by retained rows, descending
-  int E, ntn, mtiles, kdim_blocks, total;
+  int E, ntn, mtiles, kdim_blocks, total, tm;  // tm: rows of a unit's tile (128 or 256)
 };
 
 template <int MODE>
-__device__ __forceinline__ Tile decode(const Sched& s, int tau) {
+__device__ __forceinline__ Tile decode(const Sched& s, int tau, int rank) {
   Tile t;
   if constexpr (Geo<MODE>::kWgrad) {
     const int per = s.mtiles * s.ntn;
     const int r = tau / per, loc = tau - r * per;
     t.e = s.order[r];
-    t.m0 = (loc / s.ntn) * BM;
+    t.m0 = (loc / s.ntn) * s.tm;
     t.n0 = (loc % s.ntn) * BN;
     t.row0 = s.goff[t.e];
     const int m = s.goff[t.e + 1] - t.row0;
     t.nkb = (m + BK - 1) / BK;
     t.valid = m - (t.nkb - 1) * BK;
+    t.cvalid = 0;
   } else {
     int lo = 0, hi = s.E;  // largest e with tpre[e] <= tau
     while (hi - lo > 1) {
@@ -324,12 +406,14 @@ __device__ __forceinline__ Tile decode(const Sched& s, int tau) {
     t.e = lo;
     const int loc = tau - s.tpre[lo];
     const int mt = loc / s.ntn;
-    t.m0 = s.goff[lo] + mt * BM;
+    t.m0 = s.goff[lo] + mt * s.tm;
     t.n0 = (loc % s.ntn) * BN;
-    t.valid = min(BM, s.goff[lo + 1] - t.m0);
+    t.valid = min(s.tm, s.goff[lo + 1] - t.m0);
     t.nkb = s.kdim_blocks;
     t.row0 = 0;
+    t.cvalid = t.valid - rank * BM;
   }
+  t.cm0 = t.m0 + rank * BM;
   return t;
 }
 
@@ -377,16 +461,30 @@ __device__ __forceinline__ void swiglu_chunk(const uint32_t (&r)[32], const uint
 // ----------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------
-template <int MODE>
+// PAIR = false: one CTA per tile of 128 rows x 256 columns (tcgen05 cta_group::1).
+// PAIR = true:  a cluster of two CTAs per tile of 256 x 256; each CTA loads its
+//   128 A rows and half of the B rows, the even CTA issues
+//   tcgen05.mma.cta_group::2 (M = 256) for both, each CTA's tensor memory holds
+//   its 128 accumulator rows. Protocol per ring stage: both CTAs' copies land
+//   on the even CTA's full barrier (2 arrivals + bytes); its commits arrive on
+//   both CTAs' empty / accumulator-full barriers; both CTAs' epilogue warps
+//   arrive on the even CTA's accumulator-empty barrier. A weight-gradient K
+//   block whose last 16-row slice crosses the group end is the exception: the
+//   odd CTA's copy lands on its own full barrier, its (otherwise idle) MMA warp
+//   zeroes the rows past the group end and then arrives on the even CTA's.
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr bool WG = Geo<MODE>::kWgrad;
+  constexpr int BNL = Cfg<PAIR>::kBRows;
+  constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
+  constexpr int NBOX = (BM + BNL) / 64;  // 64x64 MN-major boxes per stage (wgrad)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = smem;
   const int STAGES = p.stages;
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // kEpiWarps x stage_bufs blocks
+  uint8_t* stages = smem;
+  uint8_t* staging = smem + STAGES * STB;  // kEpiWarps x stage_bufs blocks
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(staging + kEpiWarps * p.stage_bufs * STAGING_BYTES);
   uint64_t* full = bars;
@@ -405,6 +503,10 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E;
+  const int rank = PAIR ? (int)cluster_rank() : 0;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   // --- set-up: validated group offsets, tile table, barriers, TMEM -------
   if (tid == 0) {
@@ -428,6 +530,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   Sched sc;
   sc.goff = goff;
   sc.E = E;
+  sc.tm = Cfg<PAIR>::kTileRows;
   if constexpr (MODE == kG1) {
     sc.ntn = (p.H + BN - 1) / BN;
     sc.kdim_blocks = p.D / BK;
@@ -436,21 +539,21 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     sc.kdim_blocks = 2 * p.H / BK;
   } else if constexpr (MODE == kG2) {
     sc.ntn = (p.D + BN - 1) / BN;
-    sc.mtiles = (p.H + BM - 1) / BM;
+    sc.mtiles = (p.H + sc.tm - 1) / sc.tm;
   } else {
     sc.ntn = (2 * p.H + BN - 1) / BN;
-    sc.mtiles = (p.D + BM - 1) / BM;
+    sc.mtiles = (p.D + sc.tm - 1) / sc.tm;
   }
   if constexpr (WG) {
     // experts ordered by retained rows (descending, then by id): longest first
     for (int e = tid; e < E; e += kThreads) {
       const int m = goff[e + 1] - goff[e];
-      int rank = 0;
+      int rank_e = 0;
       for (int f = 0; f < E; ++f) {
         const int mf = goff[f + 1] - goff[f];
-        rank += (mf > m) || (mf == m && f < e);
+        rank_e += (mf > m) || (mf == m && f < e);
       }
-      tab[rank] = e;
+      tab[rank_e] = e;
     }
     sc.order = tab;
     sc.total = E * sc.mtiles * sc.ntn;
@@ -459,7 +562,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       int carry = 0;
       for (int base = 0; base < E; base += 32) {
         const int e = base + lane;
-        const int tiles = e < E ? ((goff[e + 1] - goff[e] + BM - 1) / BM) * sc.ntn : 0;
+        const int tiles = e < E ? ((goff[e + 1] - goff[e] + sc.tm - 1) / sc.tm) * sc.ntn : 0;
         int inc = tiles;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -475,12 +578,12 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   }
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], PAIR && leader ? 2 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 32 * kEpiWarps);
+      mbar_init(&tempty[a], kEpiWarps * (PAIR ? 2 : 1));
     }
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -491,69 +594,112 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     if (MODE == kG4) prefetch_map(mapB2);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after();
   if constexpr (!WG) sc.total = tab[E];
   const uint32_t tmem_base = *tmem_slot;
+
+  // stage s's rows [valid, 16 * ceil(valid / 16)) of every box of this CTA
+  // belong to the next group or lie past the retained rows: zero them
+  auto zero_tail = [&](uint8_t* a_s, int valid) {
+    const int zrows = 16 * ((valid + 15) >> 4) - valid;
+    uint8_t* b_s = a_s + A_BYTES;
+    for (int idx = lane; idx < zrows * NBOX * 8; idx += 32) {
+      const int c16 = idx & 7;
+      const int rz = (idx >> 3) % zrows;
+      const int bx = (idx >> 3) / zrows;
+      uint8_t* box = bx < BM / 64 ? a_s + bx * BOX_BYTES : b_s + (bx - BM / 64) * BOX_BYTES;
+      *reinterpret_cast<uint4*>(box + (valid + rz) * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
+    __syncwarp();
+  };
 
   if (warp == 0) {
     // ===================== TMA producer =====================
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
+      uint32_t tail_parity = 0;  // odd CTA of a pair: its own full barriers flip only on tails
       bool stop = false;
-      for (int tau = blockIdx.x; tau < sc.total && !stop; tau += gridDim.x) {
-        const Tile t = decode<MODE>(sc, tau);
+      for (int tau = unit; tau < sc.total && !stop; tau += units) {
+        const Tile t = decode<MODE>(sc, tau, rank);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err)) {
             stop = true;
             break;
           }
-          uint8_t* a_s = stages + stage * STAGE_BYTES;
+          uint8_t* a_s = stages + stage * STB;
           uint8_t* b_s = a_s + A_BYTES;
-          mbar_expect_tx(&full[stage], STAGE_BYTES);
+          const bool tailz = WG && kb == t.nkb - 1 && (t.valid & 15);
+          // where this CTA's copies complete: its own full barrier, or (pair,
+          // odd CTA, ordinary block) the even CTA's
+          const bool to_leader = PAIR && !leader && !tailz;
+          const uint32_t bar_cl = to_leader ? mapa(&full[stage], 0) : 0u;
+          if (!to_leader)
+            mbar_expect_tx(&full[stage], (PAIR && leader && !tailz) ? 2 * STB : STB);
+          auto load2 = [&](uint8_t* dst, const CUtensorMap* m, int x, int y) {
+            if (to_leader) tma_load_2d_pair(dst, m, bar_cl, x, y);
+            else tma_load_2d(dst, m, &full[stage], x, y);
+          };
+          auto load3 = [&](uint8_t* dst, const CUtensorMap* m, int x, int y, int z) {
+            if (to_leader) tma_load_3d_pair(dst, m, bar_cl, x, y, z);
+            else tma_load_3d(dst, m, &full[stage], x, y, z);
+          };
+          const int nb0 = t.n0 + rank * BNL;  // first B row (N) this CTA loads
           if constexpr (MODE == kG1) {
-            tma_load_2d(a_s, mapA, &full[stage], kb * BK, t.m0);
-            tma_load_3d(b_s, mapB, &full[stage], kb * BK, t.n0, t.e);
+            load2(a_s, mapA, kb * BK, t.cm0);
+            load3(b_s, mapB, kb * BK, nb0, t.e);
           } else if constexpr (MODE == kG4) {
-            tma_load_2d(a_s, mapA, &full[stage], kb * BK, t.m0);
+            load2(a_s, mapA, kb * BK, t.cm0);
             const int hb = p.H / BK;
-            if (kb < hb)
-              tma_load_3d(b_s, mapB, &full[stage], kb * BK, t.n0, t.e);
-            else
-              tma_load_3d(b_s, mapB2, &full[stage], (kb - hb) * BK, t.n0, t.e);
+            if (kb < hb) load3(b_s, mapB, kb * BK, nb0, t.e);
+            else load3(b_s, mapB2, (kb - hb) * BK, nb0, t.e);
           } else {
             const int y = t.row0 + kb * BK;
 #pragma unroll
-            for (int i = 0; i < BM / 64; ++i)
-              tma_load_2d(a_s + i * BOX_BYTES, mapA, &full[stage], t.m0 + 64 * i, y);
+            for (int i = 0; i < BM / 64; ++i) load2(a_s + i * BOX_BYTES, mapA, t.cm0 + 64 * i, y);
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(b_s + i * BOX_BYTES, mapB, &full[stage], t.n0 + 64 * i, y);
+            for (int i = 0; i < BNL / 64; ++i) load2(b_s + i * BOX_BYTES, mapB, nb0 + 64 * i, y);
           }
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
+          if (to_leader) {
+            mbar_arrive_cluster_relaxed(bar_cl);
+          } else {
+            uint32_t par = phase;
+            if (PAIR && !leader) {
+              par = (tail_parity >> stage) & 1u;
+              tail_parity ^= 1u << stage;
+            }
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (par << stage);
+          }
+          if (++stage == (uint32_t)STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      // every issued copy must land before the CTA may exit
-      for (int s = 0; s < MAX_STAGES; ++s)
+      // copies on this CTA's own barriers must land before the CTA may exit
+      // (in a pair the even CTA's barriers also count the odd CTA's bytes)
+      for (int s = 0; s < STAGES; ++s)
         if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_parity >> s) & 1u);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && (!PAIR || leader)) {
     // ===================== MMA issuer =====================
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, WG ? 1 : 0, WG ? 1 : 0);
+    constexpr uint32_t idesc = idesc_bf16(Cfg<PAIR>::kTileRows, BN, WG ? 1 : 0, WG ? 1 : 0);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool stop = false, issued_any = false;
-    for (int tau = blockIdx.x; tau < sc.total && !stop; tau += gridDim.x) {
-      const Tile t = decode<MODE>(sc, tau);
+    for (int tau = unit; tau < sc.total && !stop; tau += units) {
+      const Tile t = decode<MODE>(sc, tau, rank);
       if (t.nkb <= 0) continue;
       if (!warp_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
       tc_fence_after();
@@ -563,26 +709,12 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           stop = true;
           break;
         }
-        uint8_t* a_s = stages + stage * STAGE_BYTES;
+        uint8_t* a_s = stages + stage * STB;
         uint8_t* b_s = a_s + A_BYTES;
         const int valid = (WG && kb == t.nkb - 1) ? t.valid : BK;
         const int nks = (valid + 15) >> 4;
         if constexpr (WG) {
-          if (valid & 15) {
-            // rows [valid, 16*nks) of this block belong to the next group (or
-            // lie past the retained rows): zero them in every box
-            const int zrows = 16 * nks - valid;
-            const int nboxes = (BM + BN) / 64;
-            for (int idx = lane; idx < zrows * nboxes * 8; idx += 32) {
-              const int c16 = idx & 7;
-              const int rz = (idx >> 3) % zrows;
-              const int bx = (idx >> 3) / zrows;
-              uint8_t* box = bx < BM / 64 ? a_s + bx * BOX_BYTES : b_s + (bx - BM / 64) * BOX_BYTES;
-              *reinterpret_cast<uint4*>(box + (valid + rz) * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_async_smem();
-            __syncwarp();
-          }
+          if (valid & 15) zero_tail(a_s, valid);
         }
         tc_fence_after();
         if (lane == 0) {
@@ -598,30 +730,59 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                 ad = sw128_desc(a_addr + ks * 32, 16, 1024);
                 bd = sw128_desc(b_addr + ks * 32, 16, 1024);
               }
-              umma_bf16(d_tmem, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+              const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
+              if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+              else umma_bf16(d_tmem, ad, bd, idesc, accum);
             }
           }
-          umma_commit(&empty[stage]);
+          if constexpr (PAIR) umma_commit_pair(&empty[stage], 3);
+          else umma_commit(&empty[stage]);
         }
         issued_any = true;
         __syncwarp();
-        if (++stage == STAGES) {
+        if (++stage == (uint32_t)STAGES) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (stop) break;
-      if (lane == 0) umma_commit(&tfull[acc]);
+      if (lane == 0) {
+        if constexpr (PAIR) umma_commit_pair(&tfull[acc], 3);
+        else umma_commit(&tfull[acc]);
+      }
       __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-    // all MMAs of this CTA must finish before TMEM is released
+    // all MMAs of this CTA (pair) must finish before TMEM is released
     if (issued_any && lane == 0) {
-      umma_commit(drain);
+      if constexpr (PAIR) umma_commit_pair(drain, 1);
+      else umma_commit(drain);
       mbar_drain(drain, 0);
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // ===================== odd CTA of a pair: tail forwarder =====================
+    if constexpr (PAIR && WG) {
+      uint32_t stage = 0, tparity = 0;
+      bool stop = false;
+      for (int tau = unit; tau < sc.total && !stop; tau += units) {
+        const Tile t = decode<MODE>(sc, tau, rank);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (kb == t.nkb - 1 && (t.valid & 15)) {
+            if (!warp_wait(&full[stage], (tparity >> stage) & 1u, abort_flag, p.err)) {
+              stop = true;
+              break;
+            }
+            tparity ^= 1u << stage;
+            zero_tail(stages + stage * STB, t.valid);
+            if (lane == 0) mbar_arrive_cluster(mapa(&full[stage], 0));
+            __syncwarp();
+          }
+          if (++stage == (uint32_t)STAGES) stage = 0;
+        }
+      }
+    }
   } else {
     // ===================== epilogue (warps 2..9) =====================
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -633,6 +794,9 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     const int ncols = MODE == kG3 ? 2 * p.H : p.D;  // output width (G2, G3, G4)
     const int row_lim = MODE == kG2 ? p.H : p.D;    // output rows (G2, G3)
     uint32_t acc = 0, acc_phase = 0;
+    // accumulator-empty barrier: the even CTA's, reached remotely from the odd one
+    const uint32_t tempty_cl0 = PAIR ? mapa(&tempty[0], 0) : 0u;
+    const uint32_t tempty_cl1 = PAIR ? mapa(&tempty[1], 0) : 0u;
 
     // stage 32 accumulator columns of this warp's 32 rows and store them
     auto staged_store = [&](const uint32_t (&r)[32], const Tile& t, int col) {
@@ -644,32 +808,29 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       __syncwarp();
       if (lane == 0) {
         if constexpr (MODE == kG2) {
-          tma_store_3d(&maps.o1, blk, col, t.m0 + q * 32, t.e);
+          tma_store_3d(&maps.o1, blk, col, t.cm0 + q * 32, t.e);
         } else if constexpr (MODE == kG3) {
           if (col < p.H)
-            tma_store_3d(&maps.o1, blk, col, t.m0 + q * 32, t.e);
+            tma_store_3d(&maps.o1, blk, col, t.cm0 + q * 32, t.e);
           else
-            tma_store_3d(&maps.o2, blk, col - p.H, t.m0 + q * 32, t.e);
+            tma_store_3d(&maps.o2, blk, col - p.H, t.cm0 + q * 32, t.e);
         } else {
-          tma_store_2d(&maps.o1, blk, col, t.m0 + q * 32);
+          tma_store_2d(&maps.o1, blk, col, t.cm0 + q * 32);
         }
         bulk_commit();
       }
       if (nbuf == 2) buf ^= 1;
     };
 
-    for (int tau = blockIdx.x; tau < sc.total; tau += gridDim.x) {
-      const Tile t = decode<MODE>(sc, tau);
+    for (int tau = unit; tau < sc.total; tau += units) {
+      const Tile t = decode<MODE>(sc, tau, rank);
       if (t.nkb <= 0) {
         // expert without retained rows: its weight gradient is zero
         if constexpr (WG) {
-          if (t.m0 + q * 32 < row_lim) {
-            if (lane == 0) bulk_wait_read(0);
-            __syncwarp();
+          if (t.cm0 + q * 32 < row_lim) {
             uint32_t z[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0u;
-            buf = 0;
             for (int c = c_lo; c < c_hi; c += 32)
               if (t.n0 + c < ncols) staged_store(z, t, t.n0 + c);
           }
@@ -680,8 +841,8 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if constexpr (MODE == kG1) {
-        const bool rv = row_local < t.valid;
-        const int64_t j = (int64_t)t.m0 + row_local;
+        const bool rv = row_local < t.cvalid;
+        const int64_t j = (int64_t)t.cm0 + row_local;
         const __nv_bfloat16* arow = p.ab_c + j * 2 * p.H;
         __nv_bfloat16* drow = p.dab_c + j * 2 * p.H;
         uint4 a_cur[4], b_cur[4], a_nxt[4], b_nxt[4];
@@ -720,8 +881,8 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           }
         }
       } else {
-        const bool rows_in = WG ? (t.m0 + q * 32 < row_lim) : (q * 32 < t.valid);
-        const bool whole = WG || (q * 32 + 32 <= t.valid);  // G4: block inside the group
+        const bool rows_in = WG ? (t.cm0 + q * 32 < row_lim) : (q * 32 < t.cvalid);
+        const bool whole = WG || (q * 32 + 32 <= t.cvalid);  // G4: block inside the group
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t r[32];
@@ -731,13 +892,17 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (!rows_in || col >= ncols) continue;
           if (whole) {
             staged_store(r, t, col);
-          } else if (row_local < t.valid) {  // G4 block crossing the group end
-            store_f32x32(p.out0 + (int64_t)(t.m0 + row_local) * p.D + col, r);
+          } else if (row_local < t.cvalid) {  // G4 block crossing the group end
+            store_f32x32(p.out0 + (int64_t)(t.cm0 + row_local) * p.D + col, r);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR && !leader) mbar_arrive_cluster(acc ? tempty_cl1 : tempty_cl0);
+        else mbar_arrive(&tempty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -745,10 +910,21 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     __syncwarp();
   }
 
+  if (PAIR && *abort_flag) {
+    // an aborted pair may leave copies of the odd CTA in flight that only the
+    // even CTA's barriers count: give them time to land before smem is freed
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 100000ull) {
+    }
+  }
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -791,24 +967,64 @@ static bool make_map(CUtensorMap* m, const void* base, bool fp32, int rank, uint
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
 
-static size_t smem_bytes(int E, int stages, int stage_bufs) {
-  return 1024 + (size_t)stages * STAGE_BYTES + (size_t)kEpiWarps * stage_bufs * STAGING_BYTES +
-         128 + 16 +
-         (size_t)(2 * (E + 1) + 2) * 4;
+static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs) {
+  return 1024 + (size_t)stages * stage_bytes + (size_t)kEpiWarps * stage_bufs * STAGING_BYTES +
+         8 * (2 * MAX_STAGES + 5) + 16 + (size_t)(2 * (E + 1) + 2) * 4;
 }
 
-template <int MODE>
-static lrm_status launch_mode(const Maps& maps, Params p, int grid, cudaStream_t cs) {
-  p.stage_bufs = MODE == kG1 ? 0 : 1;
-  p.stages = smem_bytes(p.E, MAX_STAGES, p.stage_bufs) <= kSmemLimit ? MAX_STAGES : 3;
-  const size_t smem = smem_bytes(p.E, p.stages, p.stage_bufs);
+// Staging blocks per epilogue warp for fp32 outputs (two keep twice the store
+// bytes in flight at the cost of ring depth).
+#ifndef LRM_TC_STAGE_BUFS
+#define LRM_TC_STAGE_BUFS 1
+#endif
+
+template <int MODE, bool PAIR>
+static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStream_t cs) {
+  constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
+  p.stage_bufs = MODE == kG1 ? 0 : LRM_TC_STAGE_BUFS;
+  p.stages = MAX_STAGES;
+  while (p.stages > 2 && smem_bytes(p.E, p.stages, STB, p.stage_bufs) > kSmemLimit) --p.stages;
+  const size_t smem = smem_bytes(p.E, p.stages, STB, p.stage_bufs);
   if (smem > kSmemLimit) return LRM_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  auto kern = grouped_gemm_kernel<MODE, PAIR>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return LRM_ERR_CUDA;
-  grouped_gemm_kernel<MODE><<<grid, kThreads, smem, cs>>>(maps, p);
+  const int sms = num_sms();
+  const int per_unit = PAIR ? 2 : 1;
+  const int64_t units = std::max<int64_t>(1, std::min<int64_t>(tiles, sms / per_unit));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units * per_unit), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelEx(&cfg, kern, maps, p) != cudaSuccess) return LRM_ERR_CUDA;
   return launch_status();
+}
+
+// Which products run on CTA pairs (bit per mode, G1 = 1 ... G4 = 8). Pairs pay
+// off for the data-gradient products (G1, G4: +1-4% on the large layers); the
+// weight-gradient products measured as fast or faster on single CTAs.
+#ifndef LRM_TC_PAIR_MODES
+#define LRM_TC_PAIR_MODES 9
+#endif
+
+template <int MODE>
+static lrm_status launch_any(const Maps& single, const Maps& pair, const Params& p,
+                             int64_t tiles_single, int64_t tiles_pair, cudaStream_t cs) {
+  if constexpr (((LRM_TC_PAIR_MODES >> MODE) & 1) != 0)
+    return launch_mode<MODE, true>(pair, p, tiles_pair, cs);
+  else
+    return launch_mode<MODE, false>(single, p, tiles_single, cs);
 }
 
 }  // namespace tc
@@ -827,29 +1043,37 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   p.H = H;
   p.n_rows = (int)N;
   p.stage_bufs = 0;
-  p.stages = MAX_STAGES;
+  p.stages = 4;
   p.sel_off = a.sel_off;
   p.ab_c = reinterpret_cast<const __nv_bfloat16*>(a.ab_c);
   p.dab_c = reinterpret_cast<__nv_bfloat16*>(a.dab_c);
   p.out0 = nullptr;
   p.out1 = nullptr;
   p.err = a.err;
-  const int sms = num_sms();
-  auto grid_of = [&](int64_t tiles) {
-    return (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sms));
-  };
   lrm_status st = LRM_OK;
-  // K-major operands (data-gradient products): boxes of 64 x BM rows (A) and
-  // 64 x BN rows (weights, one expert per 3-D slice); MN-major operands
-  // (weight-gradient products): 64 x 64 boxes; fp32 outputs: 32 x 32 boxes.
+  // upper bounds of the tile counts (the exact ones depend on device-side sizes)
+  auto dg_tiles = [&](int tm, int ncols) {
+    return ((int64_t)N / tm + E) * ((ncols + BN - 1) / BN);
+  };
+  auto wg_tiles = [&](int tm, int mrows, int ncols) {
+    return (int64_t)E * ((mrows + tm - 1) / tm) * ((ncols + BN - 1) / BN);
+  };
+  // K-major operands (data-gradient products): 64 x 128 A boxes and 64 x 256
+  // (single CTA) or 64 x 128 (pair) weight boxes, one expert per 3-D slice;
+  // MN-major operands (weight-gradient products): 64 x 64 boxes; fp32
+  // outputs: 32 x 32 boxes.
   if (parts & kPartFc2Dgrad) {
-    Maps m;
-    if (!make_map(&m.a, a.dy_c, false, 2, 1, rows, D, 64, BM) ||
-        !make_map(&m.b, a.w_down, false, 3, E, H, D, 64, BN))
+    Maps m1, m2;
+    if (!make_map(&m1.a, a.dy_c, false, 2, 1, rows, D, 64, BM) ||
+        !make_map(&m1.b, a.w_down, false, 3, E, H, D, 64, BN) ||
+        !make_map(&m2.b, a.w_down, false, 3, E, H, D, 64, BN / 2))
       return LRM_ERR_CUDA;
-    m.b2 = m.o1 = m.o2 = m.b;
-    const int64_t tiles = ((int64_t)N / BM + E) * ((H + BN - 1) / BN);
-    if ((st = launch_mode<kG1>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
+    m2.a = m1.a;
+    m1.b2 = m1.o1 = m1.o2 = m1.b;
+    m2.b2 = m2.o1 = m2.o2 = m2.b;
+    if ((st = launch_any<kG1>(m1, m2, p, dg_tiles(BM, H), dg_tiles(2 * BM, H), a.stream)) !=
+        LRM_OK)
+      return st;
   }
   if (parts & kPartFc2Wgrad) {
     Maps m;
@@ -860,8 +1084,9 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     m.b2 = m.b;
     m.o2 = m.o1;
     p.out0 = a.dw_down;
-    const int64_t tiles = (int64_t)E * ((H + BM - 1) / BM) * ((D + BN - 1) / BN);
-    if ((st = launch_mode<kG2>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
+    if ((st = launch_any<kG2>(m, m, p, wg_tiles(BM, H, D), wg_tiles(2 * BM, H, D), a.stream)) !=
+        LRM_OK)
+      return st;
   }
   if (parts & kPartFc1Wgrad) {
     Maps m;
@@ -873,21 +1098,27 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     m.b2 = m.b;
     p.out0 = a.dw_gate;
     p.out1 = a.dw_up;
-    const int64_t tiles = (int64_t)E * ((D + BM - 1) / BM) * ((2 * H + BN - 1) / BN);
-    if ((st = launch_mode<kG3>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
+    if ((st = launch_any<kG3>(m, m, p, wg_tiles(BM, D, 2 * H), wg_tiles(2 * BM, D, 2 * H),
+                              a.stream)) != LRM_OK)
+      return st;
   }
   if (parts & kPartFc1Dgrad) {
-    Maps m;
-    if (!make_map(&m.a, a.dab_c, false, 2, 1, rows, 2 * H, 64, BM) ||
-        !make_map(&m.b, a.w_gate, false, 3, E, D, H, 64, BN) ||
-        !make_map(&m.b2, a.w_up, false, 3, E, D, H, 64, BN) ||
-        !make_map(&m.o1, a.dx_c, true, 2, 1, rows, D, 32, 32))
+    Maps m1, m2;
+    if (!make_map(&m1.a, a.dab_c, false, 2, 1, rows, 2 * H, 64, BM) ||
+        !make_map(&m1.b, a.w_gate, false, 3, E, D, H, 64, BN) ||
+        !make_map(&m1.b2, a.w_up, false, 3, E, D, H, 64, BN) ||
+        !make_map(&m2.b, a.w_gate, false, 3, E, D, H, 64, BN / 2) ||
+        !make_map(&m2.b2, a.w_up, false, 3, E, D, H, 64, BN / 2) ||
+        !make_map(&m1.o1, a.dx_c, true, 2, 1, rows, D, 32, 32))
       return LRM_ERR_CUDA;
-    m.o2 = m.o1;
+    m2.a = m1.a;
+    m1.o2 = m1.o1;
+    m2.o1 = m2.o2 = m1.o1;
     p.out0 = a.dx_c;
     p.out1 = nullptr;
-    const int64_t tiles = ((int64_t)N / BM + E) * ((D + BN - 1) / BN);
-    if ((st = launch_mode<kG4>(m, p, grid_of(tiles), a.stream)) != LRM_OK) return st;
+    if ((st = launch_any<kG4>(m1, m2, p, dg_tiles(BM, D), dg_tiles(2 * BM, D), a.stream)) !=
+        LRM_OK)
+      return st;
   }
   return st;
 }

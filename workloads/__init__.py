@@ -8,5 +8,5 @@ backward. Both the CUDA path and the CPU oracle receive the same bytes it
 produces.
 """
 
-from .configs import LayerConfig, CONFIGS, get_config  # noqa: F401
+from .configs import LayerConfig, CONFIGS, get_config, with_tokens  # noqa: F401
 from .generate import generate  # noqa: F401

@@ -61,6 +61,15 @@ CONFIGS = {
 }
 
 
+def with_tokens(cfg: LayerConfig, T: int) -> LayerConfig:
+    """The same layer recipe with T tokens (the stress cap follows T)."""
+    fields = dict(cfg.__dict__)
+    fields["T"] = T
+    if cfg.stress:
+        fields["cap"] = _stress_cap(T, cfg.K, cfg.E)
+    return LayerConfig(**fields)
+
+
 def get_config(name: str, **overrides) -> LayerConfig:
     """Look up a workload by name; keyword overrides give scaled variants."""
     base = CONFIGS[name]
