@@ -3,8 +3,9 @@
 //
 // Dispatch is a stable counting sort of the N = T*K pairs by expert id
 // ("Least-Loaded Expert Parallelism", Sec. 2.1 re-index and Alg. 4 sort of
-// the flattened indices; LRMoE Alg. 1 counts N_e). Three launches, no
-// inter-CTA waiting:
+// the flattened indices; LRMoE Alg. 1 counts N_e). Up to 2^20 pairs it is one
+// launch of one 8-CTA cluster (dispatch_fused_kernel below); beyond that,
+// three launches with no inter-CTA waiting:
 //   1. per-chunk histogram (each CTA owns kChunk consecutive pairs),
 //   2. one CTA scans counts -> off and chunk bases (expert-major),
 //   3. each CTA replays its chunk warp by warp; inside a warp, lanes that
@@ -162,6 +163,120 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int n
   }
 }
 
+// ---------------------------------------------------------------------------
+// Single-launch variant for up to kFusedMaxPairs pairs: one cluster of
+// kFusedCtas CTAs. Each CTA counts its contiguous share of the pairs per warp
+// (warp w of CTA c covers a contiguous sub-range, so warp order = pair order);
+// the CTAs read each other's per-expert counts through distributed shared
+// memory to get the expert offsets and their own bases, then replay their
+// share in order exactly like dispatch_scatter_kernel. No workspace, no
+// second launch, and the cluster barriers are hardware barriers (no spin).
+// ---------------------------------------------------------------------------
+constexpr int kFusedCtas = 8;
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr int64_t kFusedMaxPairs = 1 << 20;
+
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ int ld_peer_smem(const int32_t* local, uint32_t rank) {
+  uint32_t laddr = static_cast<uint32_t>(__cvta_generic_to_shared(local)), raddr;
+  int v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(rank));
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(raddr) : "memory");
+  return v;
+}
+
+__global__ void __cluster_dims__(kFusedCtas, 1, 1) __launch_bounds__(kFusedThreads)
+dispatch_fused_kernel(const int32_t* __restrict__ idx, int64_t N, int E,
+                      int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ off, int32_t* err) {
+  extern __shared__ int32_t sh[];
+  int32_t* wh = sh;                        // [32 warps][E]: counts, then exclusive bases
+  int32_t* cta_cnt = sh + kFusedWarps * E;  // [E] this CTA's counts (read by peers)
+  int32_t* base = cta_cnt + E;             // [E] first position of this CTA's pairs
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const uint32_t rank = cluster_ctarank();
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t per_cta = (N + kFusedCtas - 1) / kFusedCtas;
+  const int64_t per_warp = ((per_cta + kFusedWarps - 1) / kFusedWarps + 31) & ~int64_t(31);
+  const int64_t c_lo = (int64_t)rank * per_cta, c_hi = min(N, c_lo + per_cta);
+  const int64_t w_lo = min(c_hi, c_lo + w * per_warp), w_hi = min(c_hi, w_lo + per_warp);
+
+  for (int i = threadIdx.x; i < kFusedWarps * E; i += kFusedThreads) wh[i] = 0;
+  __syncthreads();
+  for (int64_t b = w_lo; b < w_hi; b += 32) {
+    const int64_t p = b + lane;
+    const bool valid = p < w_hi;
+    const int e = valid ? clamp_expert(idx[p], E, err) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (valid && lane == __ffs(peers) - 1) wh[w * E + e] += __popc(peers);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kFusedThreads) {
+    int run = 0;
+    for (int v = 0; v < kFusedWarps; ++v) {
+      const int c = wh[v * E + e];
+      wh[v * E + e] = run;
+      run += c;
+    }
+    cta_cnt[e] = run;
+  }
+  cluster_barrier();  // every CTA's counts are visible cluster-wide
+  for (int e0 = 0; e0 < E; e0 += kFusedThreads) {
+    const int e = e0 + threadIdx.x;
+    int tot = 0, before = 0;
+    if (e < E) {
+      for (uint32_t c = 0; c < kFusedCtas; ++c) {
+        const int v = ld_peer_smem(&cta_cnt[e], c);
+        tot += v;
+        if (c < rank) before += v;
+      }
+    }
+    const int excl = block_exclusive_scan(e < E ? tot : 0, warp_tot, &total);
+    __shared__ int carry;
+    if (threadIdx.x == 0 && e0 == 0) carry = 0;
+    __syncthreads();
+    if (e < E) {
+      base[e] = carry + excl + before;
+      if (rank == 0) {
+        counts[e] = tot;
+        off[e] = carry + excl;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry += total;
+    __syncthreads();
+  }
+  if (rank == 0 && threadIdx.x == 0) off[E] = (int32_t)N;
+  cluster_barrier();  // no CTA leaves while peers may still read its counts
+  for (int64_t b = w_lo; b < w_hi; b += 32) {
+    const int64_t p = b + lane;
+    const bool valid = p < w_hi;
+    int e = -1;
+    if (valid) {
+      e = idx[p];
+      e = e < 0 ? 0 : (e >= E ? E - 1 : e);
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (valid) {
+      const int pos = base[e] + wh[w * E + e] + __popc(peers & lanemask_lt());
+      perm[pos] = (int32_t)p;
+      inv[p] = pos;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) wh[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 __global__ void permute_rows_kernel(const int32_t* __restrict__ perm, int n_rows,
                                     const uint4* __restrict__ src, uint4* __restrict__ dst,
                                     int64_t vec_per_row) {
@@ -237,6 +352,16 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
     return LRM_ERR_INVALID_ARG;
   cudaStream_t cs = (cudaStream_t)stream;
   const int E = s->E;
+  if (N <= kFusedMaxPairs) {
+    const size_t shf = ((size_t)kFusedWarps * E + 2 * E) * 4;
+    if (shf > 48 * 1024 &&
+        cudaFuncSetAttribute(dispatch_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)shf) != cudaSuccess)
+      return LRM_ERR_CUDA;
+    dispatch_fused_kernel<<<kFusedCtas, kFusedThreads, shf, cs>>>(
+        topk_idx, N, E, perm, inv, counts, off, error_word(ws));
+    return launch_status();
+  }
   const int nblk = dispatch_chunks(N);
   int32_t* chunk_hist = reinterpret_cast<int32_t*>((char*)ws + kWsHeaderBytes);
   int32_t* chunk_base = chunk_hist + (int64_t)E * nblk;

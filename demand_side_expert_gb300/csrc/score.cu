@@ -5,17 +5,17 @@
 // the squared Frobenius norm of the rank-one contribution (alpha_u g_t) phi_u^T
 // to the protected FC2 weight gradient, computed without forming it.
 //
-// One warp per token: the token's cotangent row g_t is read once and its
-// squared norm kept in registers, then the K saved FC2-input rows phi_u of
-// that token (found through inv) are reduced four at a time so that twelve
-// or more 16-byte loads per lane are in flight. HBM-bound: every byte of g
-// and phi is read exactly once with 128-bit streaming loads.
+// One warp per token: the loads of the token's cotangent row g_t and of its
+// K saved FC2-input rows phi_u (found through inv, up to 8 at a time) are all
+// issued before any reduction, so some thirty 16-byte loads per lane are in
+// flight. HBM-bound: every byte of g and phi is read exactly once with
+// 128-bit streaming loads.
 #include "common.cuh"
 
 namespace lrm {
 
 constexpr int kScoreThreads = 256;
-constexpr int kRowsInFlight = 4;
+constexpr int kRowsInFlight = 8;
 
 template <typename T>
 __device__ __forceinline__ float row_sq_partial(const T* row, int n_vec, int lane) {
@@ -37,6 +37,8 @@ __device__ __forceinline__ float row_sq_partial(const T* row, int n_vec, int lan
   return s;
 }
 
+// Up to kRowsInFlight of the token's pairs are reduced per pass; the loads of
+// g_t and of all those phi rows are issued before any reduction.
 template <typename T>
 __global__ void __launch_bounds__(kScoreThreads)
 score_kernel(const T* __restrict__ g, const T* __restrict__ phi,
@@ -49,26 +51,27 @@ score_kernel(const T* __restrict__ g, const T* __restrict__ phi,
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int gv = D / V, hv = H / V;
   for (int64_t t = warp; t < ntok; t += nwarps) {
-    const float gsq = warp_sum(row_sq_partial(g + t * D, gv, lane));
+    // the token's dispatch positions, lane k holding slot k
+    int my_pos = -1;
+    if (lane < K) {
+      const int q = inv[t * K + lane];
+      if (q >= 0 && q < N) my_pos = q;
+      else flag_error(err, LRM_DEVERR_INDEX);
+    }
+    float gpart = 0.f;
     for (int k0 = 0; k0 < K; k0 += kRowsInFlight) {
       int pos[kRowsInFlight];
-      float part[kRowsInFlight];
 #pragma unroll
       for (int r = 0; r < kRowsInFlight; ++r) {
-        pos[r] = -1;
-        part[r] = 0.f;
-        if (k0 + r < K) {
-          const int q = inv[t * K + k0 + r];
-          if (q >= 0 && q < N) {
-            pos[r] = q;
-          } else if (lane == 0) {
-            flag_error(err, LRM_DEVERR_INDEX);
-          }
-        }
+        pos[r] = __shfl_sync(0xffffffffu, my_pos, (k0 + r) & 31);
+        if (k0 + r >= K) pos[r] = -1;
       }
+      float part[kRowsInFlight];
+      if (k0 == 0) gpart = row_sq_partial(g + t * D, gv, lane);  // issued with the rows
 #pragma unroll
       for (int r = 0; r < kRowsInFlight; ++r)
-        if (pos[r] >= 0) part[r] = row_sq_partial(phi + (int64_t)pos[r] * H, hv, lane);
+        part[r] = pos[r] >= 0 ? row_sq_partial(phi + (int64_t)pos[r] * H, hv, lane) : 0.f;
+      const float gsq = warp_sum(gpart);
 #pragma unroll
       for (int r = 0; r < kRowsInFlight; ++r) {
         const float psq = warp_sum(part[r]);
