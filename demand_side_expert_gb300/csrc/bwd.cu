@@ -118,3 +118,7 @@ extern "C" lrm_status lrm_expert_bwd_grouped(
   if ((st = run_parts(a, kPartAll)) != LRM_OK) return st;
   return launch_dx_gather(s, dx_c, inv, row_of_pos, dx, error_word(ws), (cudaStream_t)stream);
 }
+
+extern "C" lrm_status lrm_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+  return selftest_wait_timeout(ws, ws_bytes, (cudaStream_t)stream);
+}

@@ -70,6 +70,8 @@ struct Maps {
 };
 
 struct Params {
+  uint64_t wait_ns;  // bound of every pipeline wait
+  int selftest;      // 1: the copy warp delivers nothing (bounded-wait self-test)
   int E, D, H;
   int n_rows;      // row capacity of the compacted buffers
   int stage_bufs;  // 32x32 fp32 staging blocks per epilogue warp (0, 1 or 2)
@@ -118,13 +120,14 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
 // Bounded wait for the phase with the given parity. Returns false when the
 // CTA is aborting or after kWaitNs; a timeout raises the abort flag.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
-                                          volatile int* abort_flag, int32_t* err) {
+                                          volatile int* abort_flag, int32_t* err,
+                                          uint64_t limit_ns) {
   if (mbar_try(b, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try(b, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       flag_error(err, LRM_DEVERR_TIMEOUT);
       return false;
@@ -136,7 +139,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
 // need a converged warp). A completed phase stays observable until the
 // waiting warp itself lets the pipeline advance, so __all_sync terminates.
 __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity,
-                                          volatile int* abort_flag, int32_t* err) {
+                                          volatile int* abort_flag, int32_t* err,
+                                          uint64_t limit_ns) {
   const int lane = threadIdx.x & 31;
   uint64_t t0 = 0;
   if (lane == 0) t0 = globaltimer();
@@ -146,7 +150,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity,
     if (lane == 0) {
       if (*abort_flag) {
         give_up = 1;
-      } else if (globaltimer() - t0 > kWaitNs) {
+      } else if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         flag_error(err, LRM_DEVERR_TIMEOUT);
         give_up = 1;
@@ -588,7 +592,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && !p.selftest) {
     prefetch_map(mapA);
     prefetch_map(mapB);
     if (MODE == kG4) prefetch_map(mapB2);
@@ -626,7 +630,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 
   if (warp == 0) {
     // ===================== TMA producer =====================
-    if (lane == 0) {
+    if (lane == 0 && !p.selftest) {
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;
       uint32_t tail_parity = 0;  // odd CTA of a pair: its own full barriers flip only on tails
@@ -634,7 +638,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       for (int tau = unit; tau < sc.total && !stop; tau += units) {
         const Tile t = decode<MODE>(sc, tau, rank);
         for (int kb = 0; kb < t.nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_ns)) {
             stop = true;
             break;
           }
@@ -701,11 +705,11 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     for (int tau = unit; tau < sc.total && !stop; tau += units) {
       const Tile t = decode<MODE>(sc, tau, rank);
       if (t.nkb <= 0) continue;
-      if (!warp_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
+      if (!warp_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, p.wait_ns)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < t.nkb; ++kb) {
-        if (!warp_wait(&full[stage], phase, abort_flag, p.err)) {
+        if (!warp_wait(&full[stage], phase, abort_flag, p.err, p.wait_ns)) {
           stop = true;
           break;
         }
@@ -770,7 +774,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const Tile t = decode<MODE>(sc, tau, rank);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (kb == t.nkb - 1 && (t.valid & 15)) {
-            if (!warp_wait(&full[stage], (tparity >> stage) & 1u, abort_flag, p.err)) {
+            if (!warp_wait(&full[stage], (tparity >> stage) & 1u, abort_flag, p.err, p.wait_ns)) {
               stop = true;
               break;
             }
@@ -837,7 +841,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
         continue;
       }
-      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err)) break;
+      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if constexpr (MODE == kG1) {
@@ -1038,6 +1042,8 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   const uint64_t rows = std::max<uint64_t>(N, 1);
 
   Params p;
+  p.wait_ns = kWaitNs;
+  p.selftest = 0;
   p.E = E;
   p.D = D;
   p.H = H;
@@ -1121,6 +1127,37 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
       return st;
   }
   return st;
+}
+
+__global__ void selftest_init_kernel(int32_t* err, int32_t* sel_off) {
+  *err = 0;
+  sel_off[0] = 0;
+  sel_off[1] = 64;
+}
+
+// One grouped-GEMM CTA (FC1 dgrad, 1 expert, D = H = 64, 64 rows) whose copy
+// warp delivers nothing: the MMA warp's wait for its first operand stage must
+// give up after 20 ms, flag LRM_DEVERR_TIMEOUT, and the CTA must release its
+// tensor memory and return. Only the workspace header is touched.
+lrm_status selftest_wait_timeout(void* ws, size_t ws_bytes, cudaStream_t cs) {
+  using namespace tc;
+  if (!ws || ws_bytes < kWsHeaderBytes) return LRM_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LRM_ERR_UNSUPPORTED;
+  int32_t* err = error_word(ws);
+  int32_t* sel_off = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 64);
+  selftest_init_kernel<<<1, 1, 0, cs>>>(err, sel_off);
+  Params p = {};
+  p.wait_ns = 20000000ull;
+  p.selftest = 1;
+  p.E = 1;
+  p.D = 64;
+  p.H = 64;
+  p.n_rows = 64;
+  p.sel_off = sel_off;
+  p.err = err;
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  return launch_mode<kG4, false>(m, p, 1, cs);
 }
 
 }  // namespace lrm

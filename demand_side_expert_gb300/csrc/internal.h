@@ -31,6 +31,8 @@ enum : unsigned {
 lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts);
 // F32 path: the same products on CUDA cores.
 lrm_status launch_bwd_f32(const BwdArgs& a, unsigned parts);
+// Bounded-wait self-test of the grouped GEMM pipeline (see lrm.h).
+lrm_status selftest_wait_timeout(void* ws, size_t ws_bytes, cudaStream_t cs);
 // dx[t] = sum over kept slots of dx_c rows (deterministic, no atomics).
 lrm_status launch_dx_gather(const lrm_shape* s, const float* dx_c, const int32_t* inv,
                             const int32_t* row_of_pos, float* dx, int32_t* err,

@@ -25,7 +25,7 @@ EXPORTS = (
     "lrm_quota_from_rate", "lrm_score", "lrm_select_quota", "lrm_compact",
     "lrm_expert_bwd_grouped", "lrm_expert_fc2_dgrad", "lrm_expert_fc2_wgrad",
     "lrm_expert_fc1_wgrad", "lrm_expert_fc1_dgrad", "lrm_scatter_dx",
-    "lrm_dispatch_permute_noalloc",
+    "lrm_dispatch_permute_noalloc", "lrm_selftest_wait_timeout",
 )
 LRM_NOALLOC_MAX_CHUNK_ENTRIES = 65536
 
@@ -67,6 +67,7 @@ def _load():
         "lrm_expert_fc1_dgrad": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_scatter_dx": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_dispatch_permute_noalloc": (i32, [sp, vp, vp, vp, vp, vp, vp, vp]),
+        "lrm_selftest_wait_timeout": (i32, [vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -218,3 +219,8 @@ def lrm_dispatch_permute_noalloc(shape, topk_idx, perm, inv, counts, off, dev_er
     _check("lrm_dispatch_permute_noalloc", _lib.lrm_dispatch_permute_noalloc(
         ctypes.byref(shape), _p(topk_idx), _p(perm), _p(inv), _p(counts), _p(off),
         _p(dev_err), _s(stream)))
+
+
+def lrm_selftest_wait_timeout(ws, ws_bytes, stream=None):
+    _check("lrm_selftest_wait_timeout",
+           _lib.lrm_selftest_wait_timeout(_p(ws), ws_bytes, _s(stream)))

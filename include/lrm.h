@@ -216,6 +216,18 @@ lrm_status lrm_expert_bwd_grouped(const lrm_shape* shape, const int32_t* sel_off
                                   size_t ws_bytes, void* stream);
 
 /*
+ * Self-test of the failure detection in the grouped GEMMs (no counterpart on
+ * the pages). Every pipeline wait in those kernels is bounded; this launches
+ * one grouped-GEMM CTA whose copy warp is told to deliver nothing, so the MMA
+ * warp's wait for its first operand stage runs out after 20 ms. The CTA then
+ * ORs LRM_DEVERR_TIMEOUT into the error word, frees its tensor memory and
+ * returns; the CUDA context stays usable. It clears the error word first and
+ * writes only the first 256 bytes of ws. Read the result with
+ * lrm_get_device_error (expect LRM_DEVERR_TIMEOUT).
+ */
+lrm_status lrm_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
+
+/*
  * lrm_dispatch_permute for callers that cannot allocate device memory (the
  * paper has no counterpart; this is a deployment variant). Some callers are
  * handed only their input and output tensors, e.g. a plugin inside a host
