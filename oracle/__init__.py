@@ -18,6 +18,13 @@ from .lrm_oracle import (  # noqa: F401
     dispatch_permute,
     quota_from_rate,
     score,
+    score_variant,
+    splitmix64,
+    random_score,
+    METRIC_LRM,
+    METRIC_GRAD_SQ,
+    METRIC_GRAD_ABS,
+    METRIC_RANDOM,
     select_quota,
     compact,
     expert_bwd,

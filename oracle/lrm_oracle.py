@@ -150,6 +150,61 @@ def score(g, phi, alpha, perm, K: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Step 2 variants: the ablation's alternative selection criteria
+# ---------------------------------------------------------------------------
+METRIC_LRM, METRIC_GRAD_SQ, METRIC_GRAD_ABS, METRIC_RANDOM = 0, 1, 2, 3
+_GAMMA = 0x9E3779B97F4A7C15
+_MASK64 = (1 << 64) - 1
+
+
+def splitmix64(state: int) -> int:
+    """One output of SplitMix64 for the state AFTER its increment.
+
+    Published generator (Steele, Lea and Flood, "Fast splittable pseudorandom
+    number generators", OOPSLA 2014; Vigna's splitmix64.c): the state
+    advances by 0x9E3779B97F4A7C15 and is mixed by two xor-shift-multiply
+    rounds and a final xor-shift.
+    """
+    z = state & _MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _MASK64
+    return z ^ (z >> 31)
+
+
+def random_score(seed: int, p: int) -> float:
+    """Random criterion: output p+1 of SplitMix64 seeded with `seed`, top 24
+    bits scaled into [0, 1) (exact in float32)."""
+    z = splitmix64((seed + (p + 1) * _GAMMA) & _MASK64)
+    return float(z >> 40) * 2.0 ** -24
+
+
+def score_variant(metric: int, g, phi, alpha, perm, K: int, seed: int = 0) -> np.ndarray:
+    """Per-pair selection score under the criteria compared in [LRMoE] Sec. 4.7
+    (Table 2), in dispatch order.
+
+      METRIC_LRM       alpha_u^2 ||g_t||^2 ||phi_u||^2 (``score``)
+      METRIC_GRAD_SQ   ||g_t||_2^2                 READING of the squared-gradient-norm row
+      METRIC_GRAD_ABS  ||g_t||_1 = sum_d |g_t,d|   READING of the absolute-gradient row
+      METRIC_RANDOM    random_score(seed, p)       READING of the random-selection row
+    The gradient-only criteria use the cotangent g_t alone, so all K pairs of
+    a token score the same; Sec. 4.7 contrasts exactly that with LRM, which
+    also weighs the pair's activation phi_u.
+    """
+    perm = _i64(perm)
+    if metric == METRIC_LRM:
+        return score(g, phi, alpha, perm, K)
+    t_of_pos = perm // K
+    if metric == METRIC_GRAD_SQ:
+        g64 = _f64(g)
+        return np.sum(g64 * g64, axis=1)[t_of_pos]
+    if metric == METRIC_GRAD_ABS:
+        return np.sum(np.abs(_f64(g)), axis=1)[t_of_pos]
+    if metric == METRIC_RANDOM:
+        return np.array([random_score(seed, int(p)) for p in perm], dtype=F64)
+    raise ValueError("unknown metric")
+
+
+# ---------------------------------------------------------------------------
 # Step 3: per-expert top-q selection
 # ---------------------------------------------------------------------------
 def select_quota(R, off, quota, perm):

@@ -413,3 +413,34 @@ def test_planted_mistakes_are_caught(planted, monkeypatch):
     for pin in pins:
         with pytest.raises(AssertionError):
             pin()
+
+
+# ---------------------------------------------------------------------------
+# alternative selection criteria (LRMoE Sec. 4.7)
+# ---------------------------------------------------------------------------
+def test_splitmix64_published_outputs():
+    with open(os.path.join(GOLDEN, "splitmix64_seed0.txt")) as f:
+        rows = [line.split() for line in f if line.strip() and not line.startswith("#")]
+    for k, hexval in rows:
+        assert oracle.splitmix64(int(k) * 0x9E3779B97F4A7C15 & ((1 << 64) - 1)) == int(hexval, 16)
+    # the random score of pair p is output p+1 of the seeded generator
+    assert oracle.random_score(0, 0) == (0xe220a8397b1dcdaf >> 40) / 2 ** 24
+
+
+def test_gradient_only_criteria_closed_forms():
+    T, D, H, K = 3, 4, 5, 2
+    g = np.array([[1.0, -2.0, 0.5, 0.0], [3.0, 0.0, 0.0, -4.0], [0.25, 0.25, -0.25, 0.25]])
+    topk = np.array([[0, 1], [1, 2], [2, 0]])
+    perm, *_ = oracle.dispatch_permute(topk, 3)
+    phi = np.ones((T * K, H))
+    alpha = np.full((T, K), 0.5)
+    sq = oracle.score_variant(oracle.METRIC_GRAD_SQ, g, phi, alpha, perm, K)
+    ab = oracle.score_variant(oracle.METRIC_GRAD_ABS, g, phi, alpha, perm, K)
+    want_sq = {0: 5.25, 1: 25.0, 2: 0.25}
+    want_ab = {0: 3.5, 1: 7.0, 2: 1.0}
+    for pos, p in enumerate(perm):
+        assert sq[pos] == want_sq[p // K] and ab[pos] == want_ab[p // K]
+    lrm = oracle.score_variant(oracle.METRIC_LRM, g, phi, alpha, perm, K)
+    assert np.allclose(lrm, 0.25 * sq * H)  # alpha^2 ||g||^2 ||phi||^2 with ||phi||^2 = H
+    r = oracle.score_variant(oracle.METRIC_RANDOM, g, phi, alpha, perm, K, seed=7)
+    assert np.all((r >= 0) & (r < 1)) and len(set(r)) == T * K
