@@ -10,6 +10,8 @@
 // issued before any reduction, so some thirty 16-byte loads per lane are in
 // flight. HBM-bound: every byte of g and phi is read exactly once with
 // 128-bit streaming loads.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace lrm {
@@ -37,13 +39,45 @@ __device__ __forceinline__ float row_sq_partial(const T* row, int n_vec, int lan
   return s;
 }
 
-// Up to kRowsInFlight of the token's pairs are reduced per pass; the loads of
-// g_t and of all those phi rows are issued before any reduction.
 template <typename T>
+__device__ __forceinline__ float row_abs_partial(const T* row, int n_vec, int lane) {
+  constexpr int V = Vec16<T>::kElems;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  const uint4* r = reinterpret_cast<const uint4*>(row);
+#pragma unroll 4
+  for (int c = lane; c < n_vec; c += 32) {
+    float f[V];
+    Vec16<T>::unpack(ld_stream(r + c), f);
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] += fabsf(f[i]);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) s += acc[i];
+  return s;
+}
+
+// SplitMix64 (Steele, Lea and Flood, OOPSLA 2014): mix of the state after
+// its increment; the random criterion of pair p is output p+1 for `seed`.
+__device__ __forceinline__ float random_score(uint64_t seed, uint64_t p) {
+  uint64_t z = seed + (p + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return (float)(z >> 40) * (1.0f / 16777216.0f);
+}
+
+// Up to kRowsInFlight of the token's pairs are reduced per pass; the loads of
+// g_t and of all those phi rows are issued before any reduction. The other
+// criteria of LRMoE Sec. 4.7 read g_t only (or nothing, for the random one).
+template <typename T, int METRIC>
 __global__ void __launch_bounds__(kScoreThreads)
 score_kernel(const T* __restrict__ g, const T* __restrict__ phi,
              const float* __restrict__ alpha, const int32_t* __restrict__ inv,
-             float* __restrict__ score, int ntok, int D, int H, int K, int32_t* err) {
+             float* __restrict__ score, int ntok, int D, int H, int K, uint64_t seed,
+             int32_t* err) {
   constexpr int V = Vec16<T>::kElems;
   const int lane = threadIdx.x & 31;
   const int64_t N = (int64_t)ntok * K;
@@ -57,6 +91,19 @@ score_kernel(const T* __restrict__ g, const T* __restrict__ phi,
       const int q = inv[t * K + lane];
       if (q >= 0 && q < N) my_pos = q;
       else flag_error(err, LRM_DEVERR_INDEX);
+    }
+    if constexpr (METRIC != LRM_METRIC_LRM) {
+      float tok = 0.f;
+      if constexpr (METRIC == LRM_METRIC_GRAD_SQ)
+        tok = warp_sum(row_sq_partial(g + t * D, gv, lane));
+      if constexpr (METRIC == LRM_METRIC_GRAD_ABS)
+        tok = warp_sum(row_abs_partial(g + t * D, gv, lane));
+      if (lane < K && my_pos >= 0) {
+        if constexpr (METRIC == LRM_METRIC_RANDOM)
+          tok = random_score(seed, (uint64_t)t * K + lane);
+        score[my_pos] = tok;
+      }
+      continue;
     }
     float gpart = 0.f;
     for (int k0 = 0; k0 < K; k0 += kRowsInFlight) {
@@ -84,30 +131,69 @@ score_kernel(const T* __restrict__ g, const T* __restrict__ phi,
   }
 }
 
+template <typename T>
+static void launch_score(const lrm_shape* s, int metric, uint64_t seed, const void* g,
+                         const void* phi, const float* alpha, const int32_t* inv, float* score,
+                         int32_t* err, int blocks, cudaStream_t cs) {
+  const T* gt = (const T*)g;
+  const T* pt = (const T*)phi;
+  switch (metric) {
+    case LRM_METRIC_GRAD_SQ:
+      score_kernel<T, LRM_METRIC_GRAD_SQ><<<blocks, kScoreThreads, 0, cs>>>(
+          gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
+      break;
+    case LRM_METRIC_GRAD_ABS:
+      score_kernel<T, LRM_METRIC_GRAD_ABS><<<blocks, kScoreThreads, 0, cs>>>(
+          gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
+      break;
+    case LRM_METRIC_RANDOM:
+      score_kernel<T, LRM_METRIC_RANDOM><<<blocks, kScoreThreads, 0, cs>>>(
+          gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
+      break;
+    default:
+      score_kernel<T, LRM_METRIC_LRM><<<blocks, kScoreThreads, 0, cs>>>(
+          gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
+  }
+}
+
 }  // namespace lrm
 
 using namespace lrm;
 
-extern "C" lrm_status lrm_score(const lrm_shape* s, const void* g, const void* phi,
-                                const float* alpha, const int32_t* inv, float* score,
-                                void* ws, size_t ws_bytes, void* stream) {
+static lrm_status score_entry(const lrm_shape* s, int metric, uint64_t seed, const void* g,
+                              const void* phi, const float* alpha, const int32_t* inv,
+                              float* score, void* ws, size_t ws_bytes, void* stream) {
   lrm_status st = check_shape(s);
   if (st != LRM_OK) return st;
   if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
+  if (metric < LRM_METRIC_LRM || metric > LRM_METRIC_RANDOM) return LRM_ERR_INVALID_ARG;
   if (s->T == 0) return LRM_OK;
-  if (!g || !phi || !alpha || !inv || !score) return LRM_ERR_INVALID_ARG;
-  if (!aligned16(g) || !aligned16(phi)) return LRM_ERR_UNSUPPORTED;
+  const bool needs_g = metric != LRM_METRIC_RANDOM;
+  const bool needs_phi = metric == LRM_METRIC_LRM;
+  if (!inv || !score || (needs_g && !g) || (needs_phi && (!phi || !alpha)))
+    return LRM_ERR_INVALID_ARG;
+  if ((needs_g && !aligned16(g)) || (needs_phi && !aligned16(phi))) return LRM_ERR_UNSUPPORTED;
   const int64_t warps = s->T;
   const int64_t cap = (int64_t)num_sms() * (2048 / kScoreThreads) * (kScoreThreads / 32);
   const int blocks = (int)((std::min(warps, cap) + 7) / 8);
   cudaStream_t cs = (cudaStream_t)stream;
   if (s->dtype == LRM_BF16)
-    score_kernel<__nv_bfloat16><<<blocks, kScoreThreads, 0, cs>>>(
-        (const __nv_bfloat16*)g, (const __nv_bfloat16*)phi, alpha, inv, score, s->T, s->D,
-        s->H, s->K, error_word(ws));
+    launch_score<__nv_bfloat16>(s, metric, seed, g, phi, alpha, inv, score, error_word(ws),
+                                blocks, cs);
   else
-    score_kernel<float><<<blocks, kScoreThreads, 0, cs>>>(
-        (const float*)g, (const float*)phi, alpha, inv, score, s->T, s->D, s->H, s->K,
-        error_word(ws));
+    launch_score<float>(s, metric, seed, g, phi, alpha, inv, score, error_word(ws), blocks, cs);
   return launch_status();
+}
+
+extern "C" lrm_status lrm_score(const lrm_shape* s, const void* g, const void* phi,
+                                const float* alpha, const int32_t* inv, float* score,
+                                void* ws, size_t ws_bytes, void* stream) {
+  return score_entry(s, LRM_METRIC_LRM, 0, g, phi, alpha, inv, score, ws, ws_bytes, stream);
+}
+
+extern "C" lrm_status lrm_score_variant(const lrm_shape* s, int32_t metric, uint64_t seed,
+                                        const void* g, const void* phi, const float* alpha,
+                                        const int32_t* inv, float* score, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  return score_entry(s, metric, seed, g, phi, alpha, inv, score, ws, ws_bytes, stream);
 }

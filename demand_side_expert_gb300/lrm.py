@@ -25,8 +25,9 @@ EXPORTS = (
     "lrm_quota_from_rate", "lrm_score", "lrm_select_quota", "lrm_compact",
     "lrm_expert_bwd_grouped", "lrm_expert_fc2_dgrad", "lrm_expert_fc2_wgrad",
     "lrm_expert_fc1_wgrad", "lrm_expert_fc1_dgrad", "lrm_scatter_dx",
-    "lrm_dispatch_permute_noalloc", "lrm_selftest_wait_timeout",
+    "lrm_dispatch_permute_noalloc", "lrm_selftest_wait_timeout", "lrm_score_variant",
 )
+LRM_METRIC_LRM, LRM_METRIC_GRAD_SQ, LRM_METRIC_GRAD_ABS, LRM_METRIC_RANDOM = range(4)
 LRM_NOALLOC_MAX_CHUNK_ENTRIES = 65536
 
 
@@ -68,6 +69,7 @@ def _load():
         "lrm_scatter_dx": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_dispatch_permute_noalloc": (i32, [sp, vp, vp, vp, vp, vp, vp, vp]),
         "lrm_selftest_wait_timeout": (i32, [vp, sz, vp]),
+        "lrm_score_variant": (i32, [sp, i32, ctypes.c_uint64, vp, vp, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -224,3 +226,9 @@ def lrm_dispatch_permute_noalloc(shape, topk_idx, perm, inv, counts, off, dev_er
 def lrm_selftest_wait_timeout(ws, ws_bytes, stream=None):
     _check("lrm_selftest_wait_timeout",
            _lib.lrm_selftest_wait_timeout(_p(ws), ws_bytes, _s(stream)))
+
+
+def lrm_score_variant(shape, metric, seed, g, phi, alpha, inv, score, ws, ws_bytes, stream=None):
+    _check("lrm_score_variant", _lib.lrm_score_variant(
+        ctypes.byref(shape), metric, seed, _p(g), _p(phi), _p(alpha), _p(inv), _p(score),
+        _p(ws), ws_bytes, _s(stream)))

@@ -77,9 +77,14 @@ class RecalibratedExpertBackward:
     def quota_from_rate(self, num: int, den: int, cap: int = 0, stream=None):
         lrm.lrm_quota_from_rate(self.counts, self.E, num, den, cap, self.quota, stream)
 
-    def score_pairs(self, alpha, g, phi, stream=None):
-        lrm.lrm_score(self.shape, g, phi, alpha, self.inv, self.score, self.ws, self.ws_bytes,
-                      stream)
+    def score_pairs(self, alpha, g, phi, stream=None, metric: int = 0, seed: int = 0):
+        """LRM scores (metric 0) or one of the ablation criteria (lrm.LRM_METRIC_*)."""
+        if metric == lrm.LRM_METRIC_LRM:
+            lrm.lrm_score(self.shape, g, phi, alpha, self.inv, self.score, self.ws,
+                          self.ws_bytes, stream)
+        else:
+            lrm.lrm_score_variant(self.shape, metric, seed, g, phi, alpha, self.inv, self.score,
+                                  self.ws, self.ws_bytes, stream)
 
     def select(self, stream=None):
         lrm.lrm_select_quota(self.shape, self.score, self.off, self.quota, self.keep,
@@ -90,8 +95,9 @@ class RecalibratedExpertBackward:
                         g, ab, phi, self.dy_c, self.x_c, self.ab_c, self.phi_c, self.tok_c,
                         self.row_of_pos, self.ws, self.ws_bytes, stream)
 
-    def score_select_compact(self, alpha, x, g, ab, phi, stream=None):
-        self.score_pairs(alpha, g, phi, stream)
+    def score_select_compact(self, alpha, x, g, ab, phi, stream=None, metric: int = 0,
+                             seed: int = 0):
+        self.score_pairs(alpha, g, phi, stream, metric, seed)
         self.select(stream)
         self.compact(alpha, x, g, ab, phi, stream)
 
@@ -124,14 +130,16 @@ class RecalibratedExpertBackward:
                            self.ws_bytes, stream)
 
     def step(self, topk_idx, alpha, x, g, ab, phi, w_gate, w_up, w_down, rate=(1, 1),
-             cap: int = 0, quota: torch.Tensor | None = None, stream=None):
-        """One pass of the whole path. ab / phi are in dispatch order."""
+             cap: int = 0, quota: torch.Tensor | None = None, stream=None, metric: int = 0,
+             seed: int = 0):
+        """One pass of the whole path. ab / phi are in dispatch order; `metric`
+        picks the selection criterion (LRM by default)."""
         self.dispatch(topk_idx, stream)
         if quota is None:
             self.quota_from_rate(rate[0], rate[1], cap, stream)
         else:
             self.quota.copy_(quota)
-        self.score_select_compact(alpha, x, g, ab, phi, stream)
+        self.score_select_compact(alpha, x, g, ab, phi, stream, metric, seed)
         self.expert_bwd(w_gate, w_up, w_down, stream)
 
     def device_error(self, stream=None) -> int:

@@ -139,6 +139,29 @@ lrm_status lrm_score(const lrm_shape* shape, const void* g, const void* phi,
                      void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The selection criteria LRMoE Sec. 4.7 (Table 2) compares LRM against,
+ * computed like lrm_score and written to score [N] in dispatch order:
+ *   LRM_METRIC_LRM       alpha_u^2 ||g_t||^2 ||phi_u||^2   (= lrm_score)
+ *   LRM_METRIC_GRAD_SQ   ||g_t||_2^2       the "squared gradient norm"
+ *   LRM_METRIC_GRAD_ABS  sum_d |g_t,d|     the "absolute gradient magnitude"
+ *   LRM_METRIC_RANDOM    output p+1 of SplitMix64 seeded with `seed`, top 24
+ *                        bits as a float in [0,1): "pure random selection"
+ * The gradient-only criteria read g only (alpha and phi may be NULL); the
+ * random one reads neither (g may be NULL too). All are non-negative, so
+ * lrm_select_quota applies to them unchanged.
+ */
+typedef enum lrm_metric {
+  LRM_METRIC_LRM = 0,
+  LRM_METRIC_GRAD_SQ = 1,
+  LRM_METRIC_GRAD_ABS = 2,
+  LRM_METRIC_RANDOM = 3
+} lrm_metric;
+lrm_status lrm_score_variant(const lrm_shape* shape, int32_t metric, uint64_t seed,
+                             const void* g, const void* phi, const float* alpha,
+                             const int32_t* inv, float* score, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/*
  * Per-expert top-q selection, LRMoE Alg. 1 (TopK per expert) and Sec. 7.2
  * Prop. 7.1 (keeping the largest scores inside each expert is optimal for
  * fixed per-expert quotas). Inside each segment [off[e], off[e+1]) the q_e

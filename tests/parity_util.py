@@ -37,13 +37,14 @@ def rel_fro(a, b) -> float:
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a))
 
 
-def run_gpu(pipe, inp: dict, rate=(1, 1), cap=0, quota=None):
+def run_gpu(pipe, inp: dict, rate=(1, 1), cap=0, quota=None, metric=0, seed=0):
     """Dispatch, lay out the saved state, run the whole path. Returns (ab, phi)."""
     pipe.dispatch(inp["topk_idx"])
     ab = pipe.to_dispatch_order(inp["ab_pair"])
     phi = pipe.to_dispatch_order(inp["phi_pair"])
     pipe.step(inp["topk_idx"], inp["alpha"], inp["x"], inp["g"], ab, phi, inp["w_gate"],
-              inp["w_up"], inp["w_down"], rate=rate, cap=cap, quota=quota)
+              inp["w_up"], inp["w_down"], rate=rate, cap=cap, quota=quota, metric=metric,
+              seed=seed)
     torch.cuda.synchronize()
     return ab, phi
 

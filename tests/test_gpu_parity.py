@@ -37,13 +37,14 @@ def _to(inp, dev):
     return {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
-def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None):
-    """Every step of the path against the oracle on one seeded layer."""
+def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None, metric=0, rseed=0):
+    """Every step of the path against the oracle on one seeded layer; `metric`
+    and `rseed` pick the selection criterion and the random criterion's seed."""
     inp_cpu = generate(cfg, device="cpu", seed=seed)
     inp = _to(inp_cpu, dev)
     pipe = _pipe(cfg, dev)
     q_t = None if quota is None else torch.as_tensor(quota, dtype=torch.int32, device=dev)
-    run_gpu(pipe, inp, rate, cap, q_t)
+    run_gpu(pipe, inp, rate, cap, q_t, metric, rseed)
     assert pipe.device_error() == 0
     nin = numpy_inputs(inp_cpu)
     perm, inv, counts, off = check_dispatch(pipe, nin["topk_idx"], cfg.E)
@@ -53,9 +54,12 @@ def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None):
                           oracle.quota_from_rate(counts, rate[0], rate[1], cap)
                           if quota is None else np.asarray(quota))
     qv = to_np(pipe.quota).astype(np.int64)
-    ref_score = oracle.score(nin["g"], phi, nin["alpha"], perm, cfg.K)
+    ref_score = oracle.score_variant(metric, nin["g"], phi, nin["alpha"], perm, cfg.K, rseed)
     N = cfg.N
-    check_scores(to_np(pipe.score)[:N], ref_score)
+    if metric == oracle.METRIC_RANDOM:  # integer arithmetic: bit-exact
+        assert np.array_equal(to_np(pipe.score)[:N].astype(np.float64), ref_score)
+    else:
+        check_scores(to_np(pipe.score)[:N], ref_score)
     keep, sel_off, sel_pos = check_selection(pipe, perm, off, qv)
     check_set_agreement(keep, ref_score, off, qv)
     c = check_compaction(pipe, nin, perm, sel_off, sel_pos, ab, phi, cfg.K, cfg.dtype)
@@ -318,3 +322,53 @@ def test_split_substeps_match_one_call(dev):
         if k in ("dab_c", "dx_c"):
             got, v = got[:M], v[:M]
         assert torch.equal(got, v), k
+
+
+# ---------------------------------------------------------------------------
+# the alternative selection criteria of the ablation (LRMoE Sec. 4.7)
+# ---------------------------------------------------------------------------
+CRITERIA = [oracle.METRIC_GRAD_SQ, oracle.METRIC_GRAD_ABS, oracle.METRIC_RANDOM]
+
+
+@pytest.mark.parametrize("metric", CRITERIA)
+def test_alternative_criteria_whole_path(dev, metric):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=1024, D=320, H=192, E=12, K=3)
+    full_parity(cfg, dev, (1, 2), metric=metric, rseed=12345)
+
+
+@pytest.mark.parametrize("metric", CRITERIA)
+def test_alternative_criteria_fp32(dev, metric):
+    full_parity(get_config("tiny", T=200, D=48, H=40, E=6, K=3), dev, (3, 5), metric=metric,
+                rseed=2**64 - 1)
+
+
+@pytest.mark.parametrize("metric", CRITERIA)
+def test_full_size_alternative_criteria(dev, metric):
+    """Every score and the whole selection at the benchmark's layer size."""
+    cfg = get_config("qwen3-30b-a3b-t4k")
+    inp = generate(cfg, device=dev)
+    pipe = _pipe(cfg, dev)
+    run_gpu(pipe, inp, (3, 5), metric=metric, seed=7)
+    assert pipe.device_error() == 0
+    topk = to_np(inp["topk_idx"])
+    perm, inv, counts, off = check_dispatch(pipe, topk, cfg.E)
+    qv = oracle.quota_from_rate(counts, 3, 5)
+    ref = oracle.score_variant(metric, to_np(inp["g"]), None, None, perm, cfg.K, 7)
+    got = to_np(pipe.score)[:cfg.N]
+    if metric == oracle.METRIC_RANDOM:
+        assert np.array_equal(got.astype(np.float64), ref)
+    else:
+        check_scores(got, ref)
+    keep, _, _ = check_selection(pipe, perm, off, qv)
+    check_set_agreement(keep, ref, off, qv)
+
+
+def test_random_criterion_depends_on_seed_only(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=512, D=128, H=64, E=8, K=2)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    picks = []
+    for seed in (1, 2, 1):
+        run_gpu(pipe, inp, (1, 2), metric=oracle.METRIC_RANDOM, seed=seed)
+        picks.append(pipe.keep[:cfg.N].clone())
+    assert torch.equal(picks[0], picks[2]) and not torch.equal(picks[0], picks[1])
