@@ -444,3 +444,11 @@ def test_gradient_only_criteria_closed_forms():
     assert np.allclose(lrm, 0.25 * sq * H)  # alpha^2 ||g||^2 ||phi||^2 with ||phi||^2 = H
     r = oracle.score_variant(oracle.METRIC_RANDOM, g, phi, alpha, perm, K, seed=7)
     assert np.all((r >= 0) & (r < 1)) and len(set(r)) == T * K
+    # seed 0: pair p (wherever dispatch puts it) draws the published output p+1
+    with open(os.path.join(GOLDEN, "splitmix64_seed0.txt")) as f:
+        out = {int(k): int(v, 16) for k, v in
+               (line.split() for line in f if line.strip() and not line.startswith("#"))}
+    r0 = oracle.score_variant(oracle.METRIC_RANDOM, g, phi, alpha, perm, K, seed=0)
+    pos_of = {int(p): pos for pos, p in enumerate(perm)}
+    for p in (0, 1, 2):
+        assert r0[pos_of[p]] == (out[p + 1] >> 40) / 2 ** 24
