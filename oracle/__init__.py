@@ -33,4 +33,8 @@ from .lrm_oracle import (  # noqa: F401
     dx_gather,
     swiglu_grad,
     recalibrated_backward,
+    gather_tokens,
+    expert_fwd,
+    combine,
+    moe_forward,
 )

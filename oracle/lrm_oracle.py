@@ -433,6 +433,79 @@ def expert_bwd_masked_dense(keep, off, perm, alpha, x, g, ab, phi,
 
 
 # ---------------------------------------------------------------------------
+# Forward expert pass (produces the saved state the backward consumes)
+# ---------------------------------------------------------------------------
+def gather_tokens(x, perm, K: int) -> np.ndarray:
+    """x_disp[pos] = x[t] with t = perm[pos] // K: the token rows in dispatch
+    order, one per routed pair ([LLEP] Sec. 2.1: B' = [B_0, B_1, ...], each
+    B_i holding the tokens routed to expert i)."""
+    xd = _f64(x)
+    return xd[_i64(perm) // K]
+
+
+def expert_fwd(off, w_gate, w_up, w_down, x_disp):
+    """Per-expert SwiGLU feed-forward over the dispatch-ordered rows.
+
+    [LLEP] Sec. 2.1 ("Implementation"): one product B_i W_i per activated
+    expert over its group of rows. [LRMoE] Sec. 3.1 (design overview) and
+    Alg. 1 (FullForwardAndSaveContext): the full forward runs every routed
+    pair through its expert and keeps the intermediates the backward needs.
+    READING (as in ``swiglu_grad``): a = x W_gate[e], b = x W_up[e],
+    phi = SiLU(a) * b, y = phi W_down[e]; the saved state is [a | b] and phi.
+    Returns (ab [N,2H], phi [N,H], y [N,D]) in dispatch order.
+    """
+    off = _i64(off)
+    Wg, Wu, Wd = _f64(w_gate), _f64(w_up), _f64(w_down)
+    xd = _f64(x_disp)
+    E, D, H = Wg.shape
+    N = xd.shape[0]
+    ab = np.zeros((N, 2 * H), dtype=F64)
+    phi = np.zeros((N, H), dtype=F64)
+    y = np.zeros((N, D), dtype=F64)
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        a = xd[lo:hi] @ Wg[e]
+        b = xd[lo:hi] @ Wu[e]
+        ph = a / (1.0 + np.exp(-a)) * b
+        ab[lo:hi, :H] = a
+        ab[lo:hi, H:] = b
+        phi[lo:hi] = ph
+        y[lo:hi] = ph @ Wd[e]
+    return ab, phi, y
+
+
+def combine(y, alpha, inv, K: int) -> np.ndarray:
+    """MoE output h_t = sum_k alpha[t, k] * y[inv[t*K + k]].
+
+    [LLEP] Sec. 2.1, MoE output formula: the gated sum of the selected
+    experts' outputs (g_i = s_i for the top-K experts, no renormalisation);
+    [LRMoE] Sec. 3.1: the forward combines the expert outputs into the dense
+    representation handed to the next layer. Slots summed in ascending k.
+    """
+    yd, al, inv = _f64(y), _f64(alpha), _i64(inv)
+    T = al.shape[0]
+    out = np.zeros((T, yd.shape[1]), dtype=F64)
+    for t in range(T):
+        for k in range(K):
+            out[t] += al[t, k] * yd[inv[t * K + k]]
+    return out
+
+
+def moe_forward(topk_idx, alpha, x, w_gate, w_up, w_down, E: int):
+    """Dispatch, gather, per-expert forward and combine, end to end."""
+    idx = _i64(topk_idx)
+    T, K = idx.shape
+    perm, inv, counts, off = dispatch_permute(idx, E)
+    x_disp = gather_tokens(x, perm, K)
+    ab, phi, y = expert_fwd(off, w_gate, w_up, w_down, x_disp)
+    out = combine(y, alpha, inv, K)
+    return {"perm": perm, "inv": inv, "counts": counts, "off": off, "x_disp": x_disp,
+            "ab": ab, "phi": phi, "y": y, "out": out}
+
+
+# ---------------------------------------------------------------------------
 # The whole path
 # ---------------------------------------------------------------------------
 def recalibrated_backward(topk_idx, alpha, x, g, ab_pair, phi_pair,

@@ -452,3 +452,92 @@ def test_gradient_only_criteria_closed_forms():
     pos_of = {int(p): pos for pos, p in enumerate(perm)}
     for p in (0, 1, 2):
         assert r0[pos_of[p]] == (out[p + 1] >> 40) / 2 ** 24
+
+
+# ---------------------------------------------------------------------------
+# forward expert pass (LLEP Sec. 2.1 re-index and MoE formula; LRMoE Sec. 3.1)
+# ---------------------------------------------------------------------------
+def _per_token_moe(L):
+    """Independent h_t = sum_k alpha_tk FFN_e(x_t), one token at a time."""
+    out = np.zeros((L["T"], L["D"]))
+    for t in range(L["T"]):
+        for k in range(L["K"]):
+            e = L["topk"][t, k]
+            a = L["x"][t] @ L["wg"][e]
+            b = L["x"][t] @ L["wu"][e]
+            out[t] += L["alpha"][t, k] * ((a / (1.0 + np.exp(-a)) * b) @ L["wd"][e])
+    return out
+
+
+@pytest.mark.parametrize("T,D,H,E,K,seed", [(12, 6, 5, 4, 2, 0), (9, 4, 3, 6, 3, 1),
+                                            (1, 3, 2, 1, 1, 2)])
+def test_forward_matches_per_token_definition(T, D, H, E, K, seed):
+    L = _tiny_layer(np.random.default_rng(seed), T=T, D=D, H=H, E=E, K=K)
+    f = oracle.moe_forward(L["topk"], L["alpha"], L["x"], L["wg"], L["wu"], L["wd"], E)
+    np.testing.assert_allclose(f["out"], _per_token_moe(L), rtol=1e-12, atol=1e-14)
+    # saved state in dispatch order equals the per-pair forward of the layer
+    np.testing.assert_allclose(f["ab"][f["inv"]], L["ab"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(f["phi"][f["inv"]], L["phi"], rtol=1e-12, atol=1e-14)
+    assert np.array_equal(f["x_disp"][f["inv"]], np.repeat(L["x"], K, axis=0))
+
+
+def test_forward_gather_follows_reindex_example():
+    rows, _ = _read_golden("llep_reindex_example.txt")
+    tokens = rows["tokens"]
+    experts = np.array([int(v) for v in rows["experts"]])[:, None]
+    x = np.arange(len(tokens), dtype=float)[:, None] * np.ones((1, 3))  # row t holds t
+    perm, *_ = oracle.dispatch_permute(experts, E=8)
+    xd = oracle.gather_tokens(x, perm, 1)
+    assert [tokens[int(v)] for v in xd[:, 0]] == rows["reindexed"]
+
+
+def test_forward_is_consistent_with_backward_gradients():
+    """d/dW of sum_t g_t . h_t(W) by finite differences of moe_forward equals
+    the backward at full retention fed with moe_forward's own saved state."""
+    rng = np.random.default_rng(21)
+    L = _tiny_layer(rng, T=5, D=4, H=3, E=3, K=2)
+    f = oracle.moe_forward(L["topk"], L["alpha"], L["x"], L["wg"], L["wu"], L["wd"], L["E"])
+    b = oracle.recalibrated_backward(L["topk"], L["alpha"], L["x"], L["g"], f["ab"][f["inv"]],
+                                     f["phi"][f["inv"]], L["wg"], L["wu"], L["wd"], E=L["E"],
+                                     num=1, den=1)
+
+    def loss(**w):
+        ws = {"wg": L["wg"], "wu": L["wu"], "wd": L["wd"], "x": L["x"]}
+        ws.update(w)
+        o = oracle.moe_forward(L["topk"], L["alpha"], ws["x"], ws["wg"], ws["wu"], ws["wd"],
+                               L["E"])["out"]
+        return float(np.sum(o * L["g"]))
+
+    h = 1e-6
+    for name, G in (("wg", b["dw_gate"]), ("wu", b["dw_up"]), ("wd", b["dw_down"]),
+                    ("x", b["dx"])):
+        scale = np.abs(G).max()
+        for idx in itertools.islice(np.ndindex(G.shape), 0, None, 2):
+            wp, wm = L[name].copy(), L[name].copy()
+            wp[idx] += h
+            wm[idx] -= h
+            fd = (loss(**{name: wp}) - loss(**{name: wm})) / (2 * h)
+            assert abs(fd - G[idx]) <= 1e-6 * scale, (name, idx)
+
+
+_ORIG_EXPERT_FWD = orc.expert_fwd
+_ORIG_COMBINE = orc.combine
+
+
+def _gate_up_swapped_fwd(off, w_gate, w_up, w_down, x_disp):
+    return _ORIG_EXPERT_FWD(off, w_up, w_gate, w_down, x_disp)
+
+
+def _renormalised_combine(y, alpha, inv, K):
+    al = np.asarray(alpha, dtype=float)
+    return _ORIG_COMBINE(y, al / al.sum(1, keepdims=True), inv, K)
+
+
+@pytest.mark.parametrize("planted", ["gate_up_swap", "renormalised"])
+def test_planted_forward_mistakes_are_caught(planted, monkeypatch):
+    if planted == "gate_up_swap":
+        monkeypatch.setattr(orc, "expert_fwd", _gate_up_swapped_fwd)
+    else:
+        monkeypatch.setattr(orc, "combine", _renormalised_combine)
+    with pytest.raises(AssertionError):
+        test_forward_matches_per_token_definition(12, 6, 5, 4, 2, 0)
