@@ -17,25 +17,6 @@ lrm_status check_common(const lrm_shape* s, const void* ws, size_t ws_bytes,
   return LRM_OK;
 }
 
-// Every listed pointer non-null (row buffers may be null only when N == 0)
-// and 16-byte aligned.
-lrm_status check_ptrs(const lrm_shape* s, std::initializer_list<const void*> always,
-                      std::initializer_list<const void*> rows) {
-  for (const void* p : always) {
-    if (!p) return LRM_ERR_INVALID_ARG;
-    if (!aligned16(p)) return LRM_ERR_UNSUPPORTED;
-  }
-  const bool has_rows = (int64_t)s->T * s->K > 0;
-  for (const void* p : rows) {
-    if (!p) {
-      if (has_rows) return LRM_ERR_INVALID_ARG;
-      continue;
-    }
-    if (!aligned16(p)) return LRM_ERR_UNSUPPORTED;
-  }
-  return LRM_OK;
-}
-
 lrm_status run_parts(const BwdArgs& a, unsigned parts) {
   return a.s->dtype == LRM_BF16 ? launch_bwd_tc(a, parts) : launch_bwd_f32(a, parts);
 }

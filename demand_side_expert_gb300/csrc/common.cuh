@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
+
 #include "lrm.h"
 
 namespace lrm {
@@ -38,6 +40,25 @@ inline lrm_status check_ws(const lrm_shape* s, const void* ws, size_t ws_bytes) 
   if (!ws) return LRM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LRM_ERR_UNSUPPORTED;
   if (ws_bytes < workspace_bytes(s)) return LRM_ERR_WORKSPACE;
+  return LRM_OK;
+}
+
+// Every listed pointer non-null (row buffers may be null only when there are
+// no routed pairs) and 16-byte aligned.
+inline lrm_status check_ptrs(const lrm_shape* s, std::initializer_list<const void*> always,
+                             std::initializer_list<const void*> rows) {
+  for (const void* p : always) {
+    if (!p) return LRM_ERR_INVALID_ARG;
+    if (!aligned16(p)) return LRM_ERR_UNSUPPORTED;
+  }
+  const bool has_rows = (int64_t)s->T * s->K > 0;
+  for (const void* p : rows) {
+    if (!p) {
+      if (has_rows) return LRM_ERR_INVALID_ARG;
+      continue;
+    }
+    if (!aligned16(p)) return LRM_ERR_UNSUPPORTED;
+  }
   return LRM_OK;
 }
 

@@ -1,7 +1,9 @@
-// FP32 variant of the four expert-backward products on CUDA cores.
+// FP32 variant of the four expert-backward products and of the two forward
+// expert products on CUDA cores.
 //
 // Same arithmetic as the tensor-core path (LRMoE Alg. 1 PackedExpertBackward
-// over each expert's retained rows; m_e read from sel_off on the device),
+// over each expert's retained rows, m_e read from sel_off on the device; the
+// forward over each expert's routed rows, groups from the dispatch offsets),
 // one thread per output element with a sequential FP32 dot product. It
 // serves FP32 layers, whose sizes are small; the BF16 path is the fast one.
 #include <algorithm>
@@ -93,6 +95,68 @@ __global__ void f32_g3_kernel(const int32_t* __restrict__ sel_off, int E, int D,
     float* out = n < H ? dw_gate : dw_up;
     out[((int64_t)e * D + d) * H + (n < H ? n : n - H)] = acc;
   }
+}
+
+// F1: ab[j] = [x_j W_gate[e] | x_j W_up[e]], phi[j] = SiLU(a) * b
+__global__ void f32_f1_kernel(const int32_t* __restrict__ off, int64_t n_rows, int E, int D,
+                              int H,
+                              const float* __restrict__ x_disp, const float* __restrict__ w_gate,
+                              const float* __restrict__ w_up, float* __restrict__ ab,
+                              float* __restrict__ phi) {
+  const int64_t N = min((int64_t)off[E], n_rows);
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < N * H;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(o / H), h = (int)(o % H);
+    const int e = expert_of_row(off, E, j);
+    const float* xr = x_disp + (int64_t)j * D;
+    const float* wg = w_gate + (int64_t)e * D * H + h;
+    const float* wu = w_up + (int64_t)e * D * H + h;
+    float a = 0.f, b = 0.f;
+    for (int d = 0; d < D; ++d) {
+      a = fmaf(xr[d], wg[(int64_t)d * H], a);
+      b = fmaf(xr[d], wu[(int64_t)d * H], b);
+    }
+    ab[(int64_t)j * 2 * H + h] = a;
+    ab[(int64_t)j * 2 * H + H + h] = b;
+    phi[(int64_t)j * H + h] = a / (1.0f + expf(-a)) * b;
+  }
+}
+
+// F2: y[j, d] = sum_h phi[j,h] W_down[e][h,d]
+__global__ void f32_f2_kernel(const int32_t* __restrict__ off, int64_t n_rows, int E, int D,
+                              int H,
+                              const float* __restrict__ phi, const float* __restrict__ w_down,
+                              float* __restrict__ y) {
+  const int64_t N = min((int64_t)off[E], n_rows);
+  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < N * D;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(o / D), d = (int)(o % D);
+    const int e = expert_of_row(off, E, j);
+    const float* pr = phi + (int64_t)j * H;
+    const float* wd = w_down + (int64_t)e * H * D + d;
+    float acc = 0.f;
+    for (int h = 0; h < H; ++h) acc = fmaf(pr[h], wd[(int64_t)h * D], acc);
+    y[o] = acc;
+  }
+}
+
+static int f32_grid(int64_t work) {
+  return (int)std::max<int64_t>(1, std::min<int64_t>((work + kF32Threads - 1) / kF32Threads,
+                                                     (int64_t)num_sms() * 8));
+}
+
+lrm_status launch_fwd_f32(const FwdArgs& a, unsigned parts) {
+  const lrm_shape* s = a.s;
+  const int D = s->D, H = s->H, E = s->E;
+  const int64_t N = (int64_t)s->T * s->K;
+  if (parts & kPartFc1Fwd)
+    f32_f1_kernel<<<f32_grid(N * H), kF32Threads, 0, a.stream>>>(
+        a.off, N, E, D, H, (const float*)a.x_disp, (const float*)a.w_gate, (const float*)a.w_up,
+        (float*)a.ab, (float*)a.phi);
+  if (parts & kPartFc2Fwd)
+    f32_f2_kernel<<<f32_grid(N * D), kF32Threads, 0, a.stream>>>(
+        a.off, N, E, D, H, (const float*)a.phi, (const float*)a.w_down, (float*)a.y);
+  return launch_status();
 }
 
 lrm_status launch_bwd_f32(const BwdArgs& a, unsigned parts) {

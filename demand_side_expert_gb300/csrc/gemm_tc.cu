@@ -11,6 +11,14 @@
 //   G2  dW_down[e] = phi_c^T dy_c   [H x D], reduction over m_e.
 //   G3  [dW_gate | dW_up][e] = x_c^T dab_c   [D x 2H], reduction over m_e.
 //   G4  dx_c = da W_gate[e]^T + db W_up[e]^T   [m_e x D] (fp32).
+// The forward expert pass that produces the saved state runs on the same
+// kernel over every routed row (groups from the dispatch offsets):
+//   F1  [a | b] = x_disp [W_gate[e] | W_up[e]]   [n_e x 2H], epilogue:
+//       phi = SiLU(a) * b; writes ab and phi (bf16). A 256-column tile holds
+//       128 gate columns and the same 128 up columns, so every thread has the
+//       a and b of its outputs.
+//   F2  y = phi W_down[e]   [n_e x D] (bf16).
+// Both read the weights in their stored layout (MN-major B operands).
 //
 // Kernel shape (one CTA per SM, persistent over a device-computed tile list):
 //   warp 0    TMA producer: 128x64 A and 256x64 B tiles, 128-byte swizzle,
@@ -61,9 +69,9 @@ constexpr uint32_t STAGING_BYTES = 32 * 32 * 4;  // one 32x32 fp32 block, 128B-s
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per pipeline wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
-enum Mode { kG1 = 0, kG2 = 1, kG3 = 2, kG4 = 3 };
+enum Mode { kG1 = 0, kG2 = 1, kG3 = 2, kG4 = 3, kF1 = 4, kF2 = 5 };
 
-// Operand maps (A, B, second B for G4) and output maps (G2: dW_down,
+// Operand maps (A, B, second B for G4 and F1) and output maps (G2: dW_down,
 // G3: dW_gate and dW_up, G4: dx_c), passed by value in parameter space.
 struct Maps {
   CUtensorMap a, b, b2, o1, o2;
@@ -81,6 +89,8 @@ struct Params {
   __nv_bfloat16* dab_c;
   float* out0;
   float* out1;
+  __nv_bfloat16* ob0;  // F1: ab, F2: y
+  __nv_bfloat16* ob1;  // F1: phi
   int32_t* err;
 };
 
@@ -364,6 +374,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 template <int MODE>
 struct Geo {
   static constexpr bool kWgrad = (MODE == kG2 || MODE == kG3);
+  static constexpr bool kFwd = (MODE == kF1 || MODE == kF2);
+  static constexpr bool kAmn = kWgrad;          // A operand MN-major
+  static constexpr bool kBmn = kWgrad || kFwd;  // B operand MN-major
 };
 
 // ----------------------------------------------------------------------------
@@ -541,6 +554,12 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   } else if constexpr (MODE == kG4) {
     sc.ntn = (p.D + BN - 1) / BN;
     sc.kdim_blocks = 2 * p.H / BK;
+  } else if constexpr (MODE == kF1) {
+    sc.ntn = (p.H + BN / 2 - 1) / (BN / 2);
+    sc.kdim_blocks = p.D / BK;
+  } else if constexpr (MODE == kF2) {
+    sc.ntn = (p.D + BN - 1) / BN;
+    sc.kdim_blocks = p.H / BK;
   } else if constexpr (MODE == kG2) {
     sc.ntn = (p.D + BN - 1) / BN;
     sc.mtiles = (p.H + sc.tm - 1) / sc.tm;
@@ -595,7 +614,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   if (warp == 0 && lane == 0 && !p.selftest) {
     prefetch_map(mapA);
     prefetch_map(mapB);
-    if (MODE == kG4) prefetch_map(mapB2);
+    if (MODE == kG4 || MODE == kF1) prefetch_map(mapB2);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -668,6 +687,21 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const int hb = p.H / BK;
             if (kb < hb) load3(b_s, mapB, kb * BK, nb0, t.e);
             else load3(b_s, mapB2, (kb - hb) * BK, nb0, t.e);
+          } else if constexpr (MODE == kF1) {
+            // tile columns [0, 128): gate h0.., [128, 256): up h0..; 64 x 64 boxes
+            load2(a_s, mapA, kb * BK, t.cm0);
+            const int h0 = t.n0 / 2;
+#pragma unroll
+            for (int i = 0; i < BNL / 64; ++i) {
+              const int n = rank * BNL + 64 * i;
+              load3(b_s + i * BOX_BYTES, n < BN / 2 ? mapB : mapB2, h0 + (n & (BN / 2 - 1)),
+                    kb * BK, t.e);
+            }
+          } else if constexpr (MODE == kF2) {
+            load2(a_s, mapA, kb * BK, t.cm0);
+#pragma unroll
+            for (int i = 0; i < BNL / 64; ++i)
+              load3(b_s + i * BOX_BYTES, mapB, nb0 + 64 * i, kb * BK, t.e);
           } else {
             const int y = t.row0 + kb * BK;
 #pragma unroll
@@ -699,7 +733,8 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     }
   } else if (warp == 1 && (!PAIR || leader)) {
     // ===================== MMA issuer =====================
-    constexpr uint32_t idesc = idesc_bf16(Cfg<PAIR>::kTileRows, BN, WG ? 1 : 0, WG ? 1 : 0);
+    constexpr bool AMN = Geo<MODE>::kAmn, BMN = Geo<MODE>::kBmn;
+    constexpr uint32_t idesc = idesc_bf16(Cfg<PAIR>::kTileRows, BN, AMN ? 1 : 0, BMN ? 1 : 0);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool stop = false, issued_any = false;
     for (int tau = unit; tau < sc.total && !stop; tau += units) {
@@ -726,14 +761,12 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
             if (ks < nks) {
-              uint64_t ad, bd;
-              if constexpr (WG) {  // MN-major: 16 K-rows = 2 x 1024 B per step
-                ad = sw128_desc(a_addr + ks * 2048, BOX_BYTES, 1024);
-                bd = sw128_desc(b_addr + ks * 2048, BOX_BYTES, 1024);
-              } else {  // K-major: 16 elements = 32 B per step
-                ad = sw128_desc(a_addr + ks * 32, 16, 1024);
-                bd = sw128_desc(b_addr + ks * 32, 16, 1024);
-              }
+              // MN-major: 16 K-rows = 2 x 1024 B per step, 64-column boxes
+              // BOX_BYTES apart; K-major: 16 elements = 32 B per step
+              const uint64_t ad = AMN ? sw128_desc(a_addr + ks * 2048, BOX_BYTES, 1024)
+                                      : sw128_desc(a_addr + ks * 32, 16, 1024);
+              const uint64_t bd = BMN ? sw128_desc(b_addr + ks * 2048, BOX_BYTES, 1024)
+                                      : sw128_desc(b_addr + ks * 32, 16, 1024);
               const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
               if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
               else umma_bf16(d_tmem, ad, bd, idesc, accum);
@@ -884,6 +917,59 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             b_cur[v] = b_nxt[v];
           }
         }
+      } else if constexpr (MODE == kF1) {
+        // this warp's 64 gate columns and the matching 64 up columns
+        const bool rv = row_local < t.cvalid;
+        const int64_t j = (int64_t)t.cm0 + row_local;
+        const int hbase = ((warp - 2) >> 2) * (BN / 4);
+#pragma unroll 1
+        for (int cc = 0; cc < BN / 4; cc += 32) {
+          const int hl = hbase + cc;
+          uint32_t ra[32], rb[32];
+          tmem_ld32(taddr + hl, ra);
+          tmem_ld32(taddr + BN / 2 + hl, rb);
+          tmem_ld_wait();
+          const int h = t.n0 / 2 + hl;
+          if (rv && h < p.H) {
+            __nv_bfloat16* arow = p.ob0 + j * 2 * p.H;
+            uint4* a_dst = reinterpret_cast<uint4*>(arow + h);
+            uint4* b_dst = reinterpret_cast<uint4*>(arow + p.H + h);
+            uint4* f_dst = reinterpret_cast<uint4*>(p.ob1 + j * p.H + h);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float a[8], b[8], f[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                a[u] = __uint_as_float(ra[8 * v + u]);
+                b[u] = __uint_as_float(rb[8 * v + u]);
+                f[u] = a[u] * __fdividef(1.0f, 1.0f + __expf(-a[u])) * b[u];
+              }
+              a_dst[v] = Vec16<__nv_bfloat16>::pack(a);
+              b_dst[v] = Vec16<__nv_bfloat16>::pack(b);
+              f_dst[v] = Vec16<__nv_bfloat16>::pack(f);
+            }
+          }
+        }
+      } else if constexpr (MODE == kF2) {
+        const bool rv = row_local < t.cvalid;
+        const int64_t j = (int64_t)t.cm0 + row_local;
+#pragma unroll 1
+        for (int c = c_lo; c < c_hi; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          tmem_ld_wait();
+          const int col = t.n0 + c;
+          if (rv && col < p.D) {
+            uint4* dst = reinterpret_cast<uint4*>(p.ob0 + j * p.D + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(r[8 * v + u]);
+              dst[v] = Vec16<__nv_bfloat16>::pack(f);
+            }
+          }
+        }
       } else {
         const bool rows_in = WG ? (t.cm0 + q * 32 < row_lim) : (q * 32 < t.cvalid);
         const bool whole = WG || (q * 32 + 32 <= t.cvalid);  // G4: block inside the group
@@ -985,7 +1071,7 @@ static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs
 template <int MODE, bool PAIR>
 static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStream_t cs) {
   constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
-  p.stage_bufs = MODE == kG1 ? 0 : LRM_TC_STAGE_BUFS;
+  p.stage_bufs = (MODE == kG1 || Geo<MODE>::kFwd) ? 0 : LRM_TC_STAGE_BUFS;
   p.stages = MAX_STAGES;
   while (p.stages > 2 && smem_bytes(p.E, p.stages, STB, p.stage_bufs) > kSmemLimit) --p.stages;
   const size_t smem = smem_bytes(p.E, p.stages, STB, p.stage_bufs);
@@ -1015,11 +1101,13 @@ static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStr
   return launch_status();
 }
 
-// Which products run on CTA pairs (bit per mode, G1 = 1 ... G4 = 8). Pairs pay
-// off for the data-gradient products (G1, G4: +1-4% on the large layers); the
-// weight-gradient products measured as fast or faster on single CTAs.
+// Which products run on CTA pairs (bit per mode, G1 = 1 ... G4 = 8, F1 = 16,
+// F2 = 32). Pairs pay off where the weights are the B operand (G1, G4: +1-4%
+// on the large layers; F1, F2 likewise read each weight tile once per 256
+// rows); the weight-gradient products measured as fast or faster on single
+// CTAs.
 #ifndef LRM_TC_PAIR_MODES
-#define LRM_TC_PAIR_MODES 9
+#define LRM_TC_PAIR_MODES 57
 #endif
 
 template <int MODE>
@@ -1055,6 +1143,8 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   p.dab_c = reinterpret_cast<__nv_bfloat16*>(a.dab_c);
   p.out0 = nullptr;
   p.out1 = nullptr;
+  p.ob0 = nullptr;
+  p.ob1 = nullptr;
   p.err = a.err;
   lrm_status st = LRM_OK;
   // upper bounds of the tile counts (the exact ones depend on device-side sizes)
@@ -1124,6 +1214,54 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     p.out1 = nullptr;
     if ((st = launch_any<kG4>(m1, m2, p, dg_tiles(BM, D), dg_tiles(2 * BM, D), a.stream)) !=
         LRM_OK)
+      return st;
+  }
+  return st;
+}
+
+lrm_status launch_fwd_tc(const FwdArgs& a, unsigned parts) {
+  using namespace tc;
+  const lrm_shape* s = a.s;
+  const int D = s->D, H = s->H, E = s->E;
+  if (D % 64 != 0 || H % 64 != 0) return LRM_ERR_UNSUPPORTED;
+  const uint64_t N = (uint64_t)s->T * s->K;
+  const uint64_t rows = std::max<uint64_t>(N, 1);
+  Params p = {};
+  p.wait_ns = kWaitNs;
+  p.E = E;
+  p.D = D;
+  p.H = H;
+  p.n_rows = (int)N;
+  p.sel_off = a.off;
+  p.err = a.err;
+  lrm_status st = LRM_OK;
+  // upper bound of the tile count: every group may end in a partial tile
+  auto tiles = [&](int tm, int ntn) { return ((int64_t)N / tm + E) * ntn; };
+  // K-major activations (64 x 128 boxes) against the weights in their stored
+  // layout, read as MN-major 64 x 64 boxes, one expert per 3-D slice
+  if (parts & kPartFc1Fwd) {
+    Maps m;
+    if (!make_map(&m.a, a.x_disp, false, 2, 1, rows, D, 64, BM) ||
+        !make_map(&m.b, a.w_gate, false, 3, E, D, H, 64, 64) ||
+        !make_map(&m.b2, a.w_up, false, 3, E, D, H, 64, 64))
+      return LRM_ERR_CUDA;
+    m.o1 = m.o2 = m.b;
+    p.ob0 = reinterpret_cast<__nv_bfloat16*>(a.ab);
+    p.ob1 = reinterpret_cast<__nv_bfloat16*>(a.phi);
+    const int ntn = (H + BN / 2 - 1) / (BN / 2);
+    if ((st = launch_any<kF1>(m, m, p, tiles(BM, ntn), tiles(2 * BM, ntn), a.stream)) != LRM_OK)
+      return st;
+  }
+  if (parts & kPartFc2Fwd) {
+    Maps m;
+    if (!make_map(&m.a, a.phi, false, 2, 1, rows, H, 64, BM) ||
+        !make_map(&m.b, a.w_down, false, 3, E, H, D, 64, 64))
+      return LRM_ERR_CUDA;
+    m.b2 = m.o1 = m.o2 = m.b;
+    p.ob0 = reinterpret_cast<__nv_bfloat16*>(a.y);
+    p.ob1 = nullptr;
+    const int ntn = (D + BN - 1) / BN;
+    if ((st = launch_any<kF2>(m, m, p, tiles(BM, ntn), tiles(2 * BM, ntn), a.stream)) != LRM_OK)
       return st;
   }
   return st;

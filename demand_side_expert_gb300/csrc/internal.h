@@ -27,10 +27,30 @@ enum : unsigned {
   kPartAll = 15
 };
 
+struct FwdArgs {
+  const lrm_shape* s;
+  const int32_t* off;  // dispatch group offsets [E+1]
+  const void *w_gate, *w_up, *w_down;
+  const void* x_disp;
+  void *ab, *phi, *y;
+  int32_t* err;
+  cudaStream_t stream;
+};
+
+// Sub-steps of the forward expert pass.
+enum : unsigned {
+  kPartFc1Fwd = 1,  // [a | b] = x_disp [W_gate | W_up], phi = SiLU(a) * b
+  kPartFc2Fwd = 2,  // y = phi W_down
+  kPartFwdAll = 3
+};
+
 // BF16 path: persistent tcgen05 grouped GEMMs (tensor cores).
 lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts);
 // F32 path: the same products on CUDA cores.
 lrm_status launch_bwd_f32(const BwdArgs& a, unsigned parts);
+// Forward expert products, BF16 (tensor cores) and F32 (CUDA cores).
+lrm_status launch_fwd_tc(const FwdArgs& a, unsigned parts);
+lrm_status launch_fwd_f32(const FwdArgs& a, unsigned parts);
 // Bounded-wait self-test of the grouped GEMM pipeline (see lrm.h).
 lrm_status selftest_wait_timeout(void* ws, size_t ws_bytes, cudaStream_t cs);
 // dx[t] = sum over kept slots of dx_c rows (deterministic, no atomics).

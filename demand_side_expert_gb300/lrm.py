@@ -26,6 +26,8 @@ EXPORTS = (
     "lrm_expert_bwd_grouped", "lrm_expert_fc2_dgrad", "lrm_expert_fc2_wgrad",
     "lrm_expert_fc1_wgrad", "lrm_expert_fc1_dgrad", "lrm_scatter_dx",
     "lrm_dispatch_permute_noalloc", "lrm_selftest_wait_timeout", "lrm_score_variant",
+    "lrm_gather_tokens", "lrm_expert_fc1_fwd", "lrm_expert_fc2_fwd", "lrm_combine",
+    "lrm_expert_fwd_grouped",
 )
 LRM_METRIC_LRM, LRM_METRIC_GRAD_SQ, LRM_METRIC_GRAD_ABS, LRM_METRIC_RANDOM = range(4)
 LRM_NOALLOC_MAX_CHUNK_ENTRIES = 65536
@@ -70,6 +72,11 @@ def _load():
         "lrm_dispatch_permute_noalloc": (i32, [sp, vp, vp, vp, vp, vp, vp, vp]),
         "lrm_selftest_wait_timeout": (i32, [vp, sz, vp]),
         "lrm_score_variant": (i32, [sp, i32, ctypes.c_uint64, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_gather_tokens": (i32, [sp, vp, vp, vp, vp, sz, vp]),
+        "lrm_expert_fc1_fwd": (i32, [sp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_expert_fc2_fwd": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_combine": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_expert_fwd_grouped": (i32, [sp] + [vp] * 13 + [vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -232,3 +239,34 @@ def lrm_score_variant(shape, metric, seed, g, phi, alpha, inv, score, ws, ws_byt
     _check("lrm_score_variant", _lib.lrm_score_variant(
         ctypes.byref(shape), metric, seed, _p(g), _p(phi), _p(alpha), _p(inv), _p(score),
         _p(ws), ws_bytes, _s(stream)))
+
+
+def lrm_gather_tokens(shape, perm, x, x_disp, ws, ws_bytes, stream=None):
+    _check("lrm_gather_tokens", _lib.lrm_gather_tokens(
+        ctypes.byref(shape), _p(perm), _p(x), _p(x_disp), _p(ws), ws_bytes, _s(stream)))
+
+
+def lrm_expert_fc1_fwd(shape, off, x_disp, w_gate, w_up, ab, phi, ws, ws_bytes, stream=None):
+    _check("lrm_expert_fc1_fwd", _lib.lrm_expert_fc1_fwd(
+        ctypes.byref(shape), _p(off), _p(x_disp), _p(w_gate), _p(w_up), _p(ab), _p(phi),
+        _p(ws), ws_bytes, _s(stream)))
+
+
+def lrm_expert_fc2_fwd(shape, off, phi, w_down, y, ws, ws_bytes, stream=None):
+    _check("lrm_expert_fc2_fwd", _lib.lrm_expert_fc2_fwd(
+        ctypes.byref(shape), _p(off), _p(phi), _p(w_down), _p(y), _p(ws), ws_bytes,
+        _s(stream)))
+
+
+def lrm_combine(shape, y, alpha, inv, out, ws, ws_bytes, stream=None):
+    _check("lrm_combine", _lib.lrm_combine(
+        ctypes.byref(shape), _p(y), _p(alpha), _p(inv), _p(out), _p(ws), ws_bytes,
+        _s(stream)))
+
+
+def lrm_expert_fwd_grouped(shape, perm, inv, off, alpha, x, w_gate, w_up, w_down, x_disp, ab,
+                           phi, y, out, ws, ws_bytes, stream=None):
+    _check("lrm_expert_fwd_grouped", _lib.lrm_expert_fwd_grouped(
+        ctypes.byref(shape), _p(perm), _p(inv), _p(off), _p(alpha), _p(x), _p(w_gate),
+        _p(w_up), _p(w_down), _p(x_disp), _p(ab), _p(phi), _p(y), _p(out), _p(ws), ws_bytes,
+        _s(stream)))

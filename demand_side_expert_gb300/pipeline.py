@@ -7,6 +7,9 @@ calls of liblrm in order on one CUDA stream:
   lrm_dispatch_permute -> lrm_quota_from_rate -> lrm_score ->
   lrm_select_quota -> lrm_compact -> lrm_expert_bwd_grouped
 
+and, for the forward expert pass that produces the saved state,
+lrm_dispatch_permute -> lrm_expert_fwd_grouped.
+
 Every step of the path runs in liblrm's kernels; this class only allocates
 and passes pointers.
 """
@@ -65,6 +68,43 @@ class RecalibratedExpertBackward:
     def dispatch(self, topk_idx, stream=None):
         lrm.lrm_dispatch_permute(self.shape, topk_idx, self.perm, self.inv, self.counts,
                                  self.off, self.ws, self.ws_bytes, stream)
+
+    def _forward_buffers(self):
+        """Forward outputs, allocated on the first forward call only."""
+        if getattr(self, "x_disp", None) is None:
+            rows, dt, dev = max(self.N, 1), self.tdtype, self.device
+            self.x_disp = torch.empty(rows, self.D, dtype=dt, device=dev)
+            self.ab = torch.empty(rows, 2 * self.H, dtype=dt, device=dev)
+            self.phi = torch.empty(rows, self.H, dtype=dt, device=dev)
+            self.y = torch.empty(rows, self.D, dtype=dt, device=dev)
+            self.out = torch.empty(max(self.T, 1), self.D, dtype=torch.float32, device=dev)
+
+    def forward(self, topk_idx, alpha, x, w_gate, w_up, w_down, stream=None):
+        """Forward expert pass: dispatch, gather, gate/up + SwiGLU, down,
+        combine. Leaves the saved state in ``ab`` / ``phi`` (dispatch order)
+        and the layer output in ``out`` (float32 [T, D])."""
+        self._forward_buffers()
+        self.dispatch(topk_idx, stream)
+        lrm.lrm_expert_fwd_grouped(self.shape, self.perm, self.inv, self.off, alpha, x, w_gate,
+                                   w_up, w_down, self.x_disp, self.ab, self.phi, self.y,
+                                   self.out, self.ws, self.ws_bytes, stream)
+
+    def gather_tokens(self, x, stream=None):
+        self._forward_buffers()
+        lrm.lrm_gather_tokens(self.shape, self.perm, x, self.x_disp, self.ws, self.ws_bytes,
+                              stream)
+
+    def fc1_fwd(self, w_gate, w_up, stream=None):
+        lrm.lrm_expert_fc1_fwd(self.shape, self.off, self.x_disp, w_gate, w_up, self.ab,
+                               self.phi, self.ws, self.ws_bytes, stream)
+
+    def fc2_fwd(self, w_down, stream=None):
+        lrm.lrm_expert_fc2_fwd(self.shape, self.off, self.phi, w_down, self.y, self.ws,
+                               self.ws_bytes, stream)
+
+    def combine(self, alpha, stream=None):
+        lrm.lrm_combine(self.shape, self.y, alpha, self.inv, self.out, self.ws, self.ws_bytes,
+                        stream)
 
     def to_dispatch_order(self, rows_by_pair: torch.Tensor, stream=None) -> torch.Tensor:
         """Lay per-pair rows out in dispatch order with the current perm."""

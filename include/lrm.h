@@ -312,6 +312,54 @@ lrm_status lrm_scatter_dx(const lrm_shape* shape, const float* dx_c,
                           const int32_t* inv, const int32_t* row_of_pos,
                           float* dx, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Forward expert pass: the pass that produces the saved state the backward
+ * reads. LRMoE Sec. 3.1 (design overview) and Alg. 1
+ * (FullForwardAndSaveContext): every routed pair runs through its expert,
+ * the outputs are combined, and [a | b] and phi are kept per pair. LLEP
+ * Sec. 2.1: token rows are re-indexed into per-expert groups (the
+ * lrm_dispatch_permute order), one product per expert and group, and the
+ * MoE output is the routing-weighted sum h_t = sum_k alpha_tk y_(t,k).
+ * SwiGLU experts: a = x W_gate[e], b = x W_up[e], phi = SiLU(a) * b,
+ * y = phi W_down[e]. FP32 accumulation; [a | b], phi and y are rounded once
+ * to the layer dtype (phi from the unrounded a and b).
+ * Groups come from `off` (lrm_dispatch_permute), read on the device; every
+ * routed row is processed. BF16 layers need D and H multiples of 64.
+ *
+ * lrm_gather_tokens: x_disp[pos] = x[perm[pos] / K].
+ *   perm [N] int32 (read); x [T,D] dtype (read); x_disp [N,D] dtype (written).
+ *   perm entries outside [0,N) skip the row and flag LRM_DEVERR_INDEX.
+ * lrm_expert_fc1_fwd: ab [N,2H] = [a | b] and phi [N,H] (dtype, written)
+ *   from x_disp [N,D] and W_gate, W_up [E,D,H] (dtype, read).
+ * lrm_expert_fc2_fwd: y [N,D] dtype (written) from phi [N,H] and
+ *   W_down [E,H,D] (dtype, read).
+ * lrm_combine: out [T,D] float (written) = sum over slots k ascending of
+ *   alpha[t,k] * y[inv[t*K+k]]; alpha [T,K] float, inv [N] int32 (read).
+ *   Needs K <= 32.
+ * lrm_expert_fwd_grouped: the four in order, on one stream.
+ * Buffers are caller-owned device memory, 16-byte aligned, not overlapping.
+ * Sizes whose off[E] exceeds N, or non-monotone off, process no rows and
+ * flag LRM_DEVERR_INDEX. Host argument errors return before any launch.
+ */
+lrm_status lrm_gather_tokens(const lrm_shape* shape, const int32_t* perm, const void* x,
+                             void* x_disp, void* ws, size_t ws_bytes, void* stream);
+lrm_status lrm_expert_fc1_fwd(const lrm_shape* shape, const int32_t* off,
+                              const void* x_disp, const void* w_gate, const void* w_up,
+                              void* ab, void* phi, void* ws, size_t ws_bytes,
+                              void* stream);
+lrm_status lrm_expert_fc2_fwd(const lrm_shape* shape, const int32_t* off, const void* phi,
+                              const void* w_down, void* y, void* ws, size_t ws_bytes,
+                              void* stream);
+lrm_status lrm_combine(const lrm_shape* shape, const void* y, const float* alpha,
+                       const int32_t* inv, float* out, void* ws, size_t ws_bytes,
+                       void* stream);
+lrm_status lrm_expert_fwd_grouped(const lrm_shape* shape, const int32_t* perm,
+                                  const int32_t* inv, const int32_t* off, const float* alpha,
+                                  const void* x, const void* w_gate, const void* w_up,
+                                  const void* w_down, void* x_disp, void* ab, void* phi,
+                                  void* y, float* out, void* ws, size_t ws_bytes,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,36 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(lib.EXPORTS) == declared
 
 
+def _declared_params():
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(lrm_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        out[m.group(1)] = [] if params == ["void"] else params
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every ctypes argtypes list has the header's arity and argument kinds."""
+    decl = _declared_params()
+    assert sorted(decl) == sorted(lib.EXPORTS)
+    for name, params in decl.items():
+        argtypes = getattr(lib._lib, name).argtypes
+        assert len(argtypes) == len(params), (name, len(argtypes), len(params))
+        for p, a in zip(params, argtypes):
+            if "*" in p:
+                assert a is ctypes.c_void_p or hasattr(a, "_type_") and a.__name__.startswith(
+                    "LP_"), (name, p, a)
+            elif p.startswith("size_t"):
+                assert a is ctypes.c_size_t, (name, p, a)
+            elif p.startswith("uint64_t"):
+                assert a is ctypes.c_uint64, (name, p, a)
+            elif p.startswith("int64_t"):
+                assert a is ctypes.c_int64, (name, p, a)
+            else:
+                assert a is ctypes.c_int32, (name, p, a)
+
+
 def test_workspace_query_is_pure_host(lib):
     s = lib.make_shape(4096, 2048, 768, 128, 8, lib.LRM_BF16)
     b = lib.lrm_workspace_bytes(s)

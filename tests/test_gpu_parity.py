@@ -37,10 +37,13 @@ def _to(inp, dev):
     return {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
-def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None, metric=0, rseed=0):
+def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None, metric=0, rseed=0,
+                inp_cpu=None):
     """Every step of the path against the oracle on one seeded layer; `metric`
-    and `rseed` pick the selection criterion and the random criterion's seed."""
-    inp_cpu = generate(cfg, device="cpu", seed=seed)
+    and `rseed` pick the selection criterion and the random criterion's seed;
+    `inp_cpu` replaces the generated layer."""
+    if inp_cpu is None:
+        inp_cpu = generate(cfg, device="cpu", seed=seed)
     inp = _to(inp_cpu, dev)
     pipe = _pipe(cfg, dev)
     q_t = None if quota is None else torch.as_tensor(quota, dtype=torch.int32, device=dev)
