@@ -46,6 +46,13 @@ KERNEL_NAMES = {
     "scatter_dx": "dx_gather_kernel",
 }
 FUSED_DISPATCH_MAX_PAIRS = 1 << 20  # above it dispatch takes three launches
+# the forward expert pass that produces the saved state, timed on its own
+FWD_SEGMENTS = ["dispatch", "gather", "fc1_fwd", "fc2_fwd", "combine"]
+FWD_KERNEL_NAMES = {
+    "dispatch": "dispatch_fused_kernel", "gather": "gather_tokens_kernel",
+    "fc1_fwd": "grouped_gemm_kernel<4, 1>", "fc2_fwd": "grouped_gemm_kernel<5, 1>",
+    "combine": "combine_kernel",
+}
 
 
 def kernels_per_step(N: int) -> int:
@@ -75,6 +82,8 @@ def parse_args():
                     "(a scaled variant; the workload name records them)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-forward", action="store_true",
+                    help="skip the separate timing of the forward expert pass")
     return ap.parse_args()
 
 
@@ -100,6 +109,37 @@ def algorithmic(cfg, M: int) -> dict:
         "fc1_dgrad": {"bytes": M * 2 * H * s + 2 * W + M * D * 4, "flops": 4 * M * D * H},
         "scatter_dx": {"bytes": M * D * 4 + T * D * 4 + 8 * N},
     }
+
+
+def algorithmic_fwd(cfg) -> dict:
+    """Bytes (and flops) each forward segment must move at minimum, per launch."""
+    T, D, H, E, K = cfg.T, cfg.D, cfg.H, cfg.E, cfg.K
+    N = T * K
+    s = 2 if cfg.dtype == "bf16" else 4
+    W = E * D * H * s
+    return {
+        "dispatch": {"bytes": 4 * N + 8 * N + 8 * E},
+        "gather": {"bytes": T * D * s + N * D * s + 4 * N},
+        "fc1_fwd": {"bytes": N * D * s + 2 * W + N * 3 * H * s, "flops": 4 * N * D * H},
+        "fc2_fwd": {"bytes": N * H * s + W + N * D * s, "flops": 2 * N * D * H},
+        "combine": {"bytes": N * D * s + 8 * N + T * D * 4},
+    }
+
+
+def roofline_of(a: dict, ms: float, peaks: dict) -> dict:
+    """Bound, achieved and fraction of one kernel from its algorithmic work."""
+    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = a.get("flops", 0) / (peaks["bf16_tflops"] * 1e12)
+    if t_tc > t_hbm:
+        achieved = a["flops"] / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        achieved = a["bytes"] / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(achieved / roof["peak"], 4)
+    return roof
 
 
 def load_peaks():
@@ -308,6 +348,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(pipe, inp, ab, phi, rate, cfg, flush, stream, args)
+    fwd = None
+    if not args.no_forward:
+        fwd = run_forward(pipe, inp, cfg, flush, stream, args)
 
     if rank != 0:
         return None
@@ -326,17 +369,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dominant = max(SEGMENTS, key=lambda s: statistics.mean(seg_ms[s]))
     dom_ms = statistics.mean(seg_ms[dominant])
     a = alg[dominant]
-    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = a.get("flops", 0) / (peaks["bf16_tflops"] * 1e12)
-    if t_tc > t_hbm:
-        achieved = a["flops"] / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        achieved = a["bytes"] / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = round(achieved / roof["peak"], 4)
+    roof = roofline_of(a, dom_ms, peaks)
     roof["traffic"] = traffic.get(dominant)
     roof["kernel"] = KERNEL_NAMES[dominant]
     roof["algorithmic_bytes"] = a["bytes"]
@@ -382,7 +415,68 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if fwd is not None:
+        line["forward"] = fwd
     return line, cfg, rate
+
+
+def run_forward(pipe, inp, cfg, flush, stream, args):
+    """The forward expert pass that produces the saved state (dispatch, token
+    gather, gate/up products with the SwiGLU epilogue, down products, combine)
+    timed on its own with the same L2 flush and CUDA events. Reported beside
+    the backward line; it is not part of the step the headline times."""
+    import torch
+
+    def step(ev):
+        ev[0].record(stream)
+        pipe.dispatch(inp["topk_idx"])
+        ev[1].record(stream)
+        pipe.gather_tokens(inp["x"])
+        ev[2].record(stream)
+        pipe.fc1_fwd(inp["w_gate"], inp["w_up"])
+        ev[3].record(stream)
+        pipe.fc2_fwd(inp["w_down"])
+        ev[4].record(stream)
+        pipe.combine(inp["alpha"])
+        ev[5].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(len(FWD_SEGMENTS) + 1)]
+
+    pipe.gather_tokens(inp["x"])  # allocates the forward buffers
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step(new_events())
+    torch.cuda.synchronize()
+    events = [new_events() for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(1)
+        step(events[i])
+    torch.cuda.synchronize()
+    if pipe.device_error() != 0:
+        raise RuntimeError(f"device error word {pipe.device_error()} in the forward")
+    seg = {s: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in events)
+           for j, s in enumerate(FWD_SEGMENTS)}
+    ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in events)
+    alg = algorithmic_fwd(cfg)
+    peaks = load_peaks()
+    kernels = {}
+    for s in FWD_SEGMENTS:
+        k = {"ms": round(seg[s], 4), "kernels": FWD_KERNEL_NAMES[s],
+             "gbs": round(alg[s]["bytes"] / (seg[s] * 1e-3) / 1e9, 1)}
+        if "flops" in alg[s]:
+            k["tflops"] = round(alg[s]["flops"] / (seg[s] * 1e-3) / 1e12, 1)
+        kernels[s] = k
+    dominant = max(FWD_SEGMENTS, key=lambda s: seg[s])
+    roof = roofline_of(alg[dominant], seg[dominant], peaks)
+    roof["kernel"] = FWD_KERNEL_NAMES[dominant]
+    roof["traffic"] = None
+    return {"metric": "routed rows through the forward expert pass per second",
+            "value": round(cfg.N / (ms * 1e-3), 1), "unit": "rows/s",
+            "ms_per_step": round(ms, 4), "steps": args.steps,
+            "gpu_launches": (len(FWD_SEGMENTS) - 1 + (1 if cfg.N <= FUSED_DISPATCH_MAX_PAIRS
+                                                      else 3)) * args.steps,
+            "kernels": kernels, "roofline": roof}
 
 
 def run_e2e(pipe, inp, ab, phi, rate, cfg, flush, stream, args):
