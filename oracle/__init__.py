@@ -37,4 +37,5 @@ from .lrm_oracle import (  # noqa: F401
     expert_fwd,
     combine,
     moe_forward,
+    recompute_ab,
 )

@@ -506,12 +506,38 @@ def moe_forward(topk_idx, alpha, x, w_gate, w_up, w_down, E: int):
 
 
 # ---------------------------------------------------------------------------
+# Retained-only recompute of the FC1 outputs
+# ---------------------------------------------------------------------------
+def recompute_ab(sel_off, w_gate, w_up, x_c):
+    """[a | b] of the retained rows rebuilt from their token rows during the
+    backward instead of read from saved state.
+
+    RelayMoE Sec. 3.3 (memory-efficient MoE recomputation, Fig. 8): the
+    backward reconstructs the expert intermediates it needs, consumes them
+    and releases them. [LRMoE] Sec. 3.1: FC2, the activation and FC1 use the
+    same retained identities, so only retained rows are rebuilt.
+    a = x_c W_gate[e], b = x_c W_up[e] per expert segment of the compacted rows.
+    """
+    sel_off = _i64(sel_off)
+    Wg, Wu = _f64(w_gate), _f64(w_up)
+    xc = _f64(x_c)
+    E, D, H = Wg.shape
+    ab = np.zeros((xc.shape[0], 2 * H), dtype=F64)
+    for e in range(E):
+        lo, hi = int(sel_off[e]), int(sel_off[e + 1])
+        if hi > lo:
+            ab[lo:hi, :H] = xc[lo:hi] @ Wg[e]
+            ab[lo:hi, H:] = xc[lo:hi] @ Wu[e]
+    return ab
+
+
+# ---------------------------------------------------------------------------
 # The whole path
 # ---------------------------------------------------------------------------
 def recalibrated_backward(topk_idx, alpha, x, g, ab_pair, phi_pair,
                           w_gate, w_up, w_down, E: int,
                           num: int | None = None, den: int | None = None,
-                          cap: int | None = None, quota=None):
+                          cap: int | None = None, quota=None, recompute: bool = False):
     """Dispatch, score, select, compact and expert backward, end to end.
 
     [LRMoE] Alg. 1: forward counts N_e (admission), backward computes v_p,
@@ -522,18 +548,24 @@ def recalibrated_backward(topk_idx, alpha, x, g, ab_pair, phi_pair,
     ab_pair / phi_pair hold the saved state per pair index p (token-major);
     it is laid out in dispatch order here, as the forward expert products
     produced it ([LLEP] Sec. 2.1 re-index). Either a rate (num/den, cap) or
-    an explicit per-expert ``quota`` is given.
+    an explicit per-expert ``quota`` is given. With ``recompute`` the
+    retained rows' [a | b] come from ``recompute_ab`` instead of ab_pair
+    (which may then be None).
     """
     idx = _i64(topk_idx)
     T, K = idx.shape
     perm, inv, counts, off = dispatch_permute(idx, E)
-    ab = permute_rows(_f64(ab_pair), perm)
     phi = permute_rows(_f64(phi_pair), perm)
+    H = phi.shape[1]
+    ab = (np.zeros((perm.shape[0], 2 * H)) if recompute
+          else permute_rows(_f64(ab_pair), perm))
     if quota is None:
         quota = quota_from_rate(counts, num, den, cap)
     R = score(g, phi, alpha, perm, K)
     keep, sel_off, sel_pos = select_quota(R, off, quota, perm)
     c = compact(perm, sel_off, sel_pos, alpha, x, g, ab, phi, K)
+    if recompute:
+        c["ab_c"] = recompute_ab(sel_off, w_gate, w_up, c["x_c"])
     b = expert_bwd(sel_off, w_gate, w_up, w_down,
                    c["dy_c"], c["x_c"], c["ab_c"], c["phi_c"])
     dx = dx_gather(b["dx_c"], inv, c["row_of_pos"], T, K)

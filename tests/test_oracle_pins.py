@@ -541,3 +541,29 @@ def test_planted_forward_mistakes_are_caught(planted, monkeypatch):
         monkeypatch.setattr(orc, "combine", _renormalised_combine)
     with pytest.raises(AssertionError):
         test_forward_matches_per_token_definition(12, 6, 5, 4, 2, 0)
+
+
+# ---------------------------------------------------------------------------
+# retained-only recompute (RelayMoE Sec. 3.3)
+# ---------------------------------------------------------------------------
+def test_recompute_rebuilds_the_saved_rows_of_retained_pairs():
+    L = _tiny_layer(np.random.default_rng(31), T=14, D=5, H=4, E=4, K=2)
+    out = _full_backward(L, 1, 2)
+    ab_c = oracle.recompute_ab(out["sel_off"], L["wg"], L["wu"], out["x_c"])
+    # the per-pair forward of the layer (an explicit loop), retained rows only
+    np.testing.assert_allclose(ab_c, out["ab_c"], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("num,den", [(1, 2), (3, 5), (1, 1)])
+def test_backward_with_recompute_equals_saved_state_backward(num, den):
+    L = _tiny_layer(np.random.default_rng(num + 7 * den), T=16, D=6, H=5, E=4, K=2)
+    saved = _full_backward(L, num, den)
+    rec = oracle.recalibrated_backward(L["topk"], L["alpha"], L["x"], L["g"], None, L["phi"],
+                                       L["wg"], L["wu"], L["wd"], E=L["E"], num=num, den=den,
+                                       recompute=True)
+    for k in ("dw_gate", "dw_up", "dw_down", "dx"):
+        np.testing.assert_allclose(rec[k], saved[k], rtol=1e-12, atol=1e-14)
+    # a layer whose saved [a | b] disagree with x: the two paths must differ
+    bad = dict(L, ab=L["ab"] + 0.5)
+    off = _full_backward(bad, num, den)
+    assert not np.allclose(off["dw_gate"], rec["dw_gate"])
