@@ -84,6 +84,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-forward", action="store_true",
                     help="skip the separate timing of the forward expert pass")
+    ap.add_argument("--no-recompute", action="store_true",
+                    help="skip the timing of the backward step that recomputes [a | b]")
     return ap.parse_args()
 
 
@@ -351,6 +353,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     fwd = None
     if not args.no_forward:
         fwd = run_forward(pipe, inp, cfg, flush, stream, args)
+    rec = None
+    if not args.no_recompute:
+        rec = run_recompute(pipe, inp, phi, rate, cfg, flush, stream, args)
 
     if rank != 0:
         return None
@@ -417,7 +422,58 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line["e2e"] = e2e
     if fwd is not None:
         line["forward"] = fwd
+    if rec is not None:
+        line["recompute"] = rec
     return line, cfg, rate
+
+
+def run_recompute(pipe, inp, phi, rate, cfg, flush, stream, args):
+    """The same backward step without saved [a | b]: compaction copies no
+    [a | b] rows and the gate/up product rebuilds them for the retained rows
+    only (lrm_expert_fc1_recompute), then the four products and the scatter.
+    Timed like the headline step; reported beside it."""
+    import torch
+
+    def step(ev):
+        ev[0].record(stream)
+        pipe.dispatch(inp["topk_idx"])
+        pipe.quota_from_rate(rate[0], rate[1], cfg.cap)
+        pipe.score_pairs(inp["alpha"], inp["g"], phi)
+        pipe.select()
+        pipe.compact(inp["alpha"], inp["x"], inp["g"], None, phi)
+        ev[1].record(stream)
+        pipe.fc1_recompute(inp["w_gate"], inp["w_up"])
+        ev[2].record(stream)
+        pipe.expert_bwd(inp["w_gate"], inp["w_up"], inp["w_down"])
+        ev[3].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step(new_events())
+    torch.cuda.synchronize()
+    events = [new_events() for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(1)
+        step(events[i])
+    torch.cuda.synchronize()
+    if pipe.device_error() != 0:
+        raise RuntimeError(f"device error word {pipe.device_error()} in the recompute step")
+    M = pipe.retained_rows
+    ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in events)
+    rec_ms = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in events)
+    s = 2 if cfg.dtype == "bf16" else 4
+    a = {"bytes": M * cfg.D * s + 2 * cfg.E * cfg.D * cfg.H * s + M * 2 * cfg.H * s,
+         "flops": 4 * M * cfg.D * cfg.H}
+    roof = roofline_of(a, rec_ms, load_peaks())
+    roof["kernel"] = "grouped_gemm_kernel<4, 1>"
+    return {"metric": "retained rows through the backward step per second, [a | b] recomputed",
+            "value": round(M / (ms * 1e-3), 1), "unit": "rows/s", "ms_per_step": round(ms, 4),
+            "steps": args.steps, "saved_state_bytes_avoided": cfg.N * 2 * cfg.H * s,
+            "recompute_ms": round(rec_ms, 4), "recompute_roofline": roof,
+            "gpu_launches": (kernels_per_step(cfg.N) + 1) * args.steps}
 
 
 def run_forward(pipe, inp, cfg, flush, stream, args):

@@ -7,6 +7,9 @@
 // phi, in dispatch order). LLEP Sec. 2.1: the token rows are re-indexed into
 // per-expert groups, each group runs one product per expert, and the MoE
 // output is the routing-weighted sum of the selected experts' outputs.
+// The gate/up product also serves the retained-only recompute of the
+// backward (RelayMoE Sec. 3.3): run over the compacted rows, it rebuilds
+// [a | b] of the retained pairs without saved state.
 #include <algorithm>
 
 #include "common.cuh"
@@ -183,4 +186,17 @@ extern "C" lrm_status lrm_expert_fwd_grouped(const lrm_shape* s, const int32_t* 
   FwdArgs a{s, off, w_gate, w_up, w_down, x_disp, ab, phi, y, error_word(ws), cs};
   if ((st = run_fwd(a, kPartFwdAll)) != LRM_OK) return st;
   return launch_combine(s, y, alpha, inv, out, error_word(ws), cs);
+}
+
+extern "C" lrm_status lrm_expert_fc1_recompute(const lrm_shape* s, const int32_t* sel_off,
+                                               const void* x_c, const void* w_gate,
+                                               const void* w_up, void* ab_c, void* ws,
+                                               size_t ws_bytes, void* stream) {
+  lrm_status st = check_base(s, ws, ws_bytes);
+  if (st != LRM_OK) return st;
+  if ((st = check_ptrs(s, {sel_off, w_gate, w_up}, {x_c, ab_c})) != LRM_OK) return st;
+  if ((int64_t)s->T * s->K == 0) return LRM_OK;
+  FwdArgs a{s, sel_off, w_gate, w_up, nullptr, x_c, ab_c, nullptr, nullptr, error_word(ws),
+            (cudaStream_t)stream};
+  return run_fwd(a, kPartFc1Fwd);
 }

@@ -118,7 +118,7 @@ __global__ void f32_f1_kernel(const int32_t* __restrict__ off, int64_t n_rows, i
     }
     ab[(int64_t)j * 2 * H + h] = a;
     ab[(int64_t)j * 2 * H + H + h] = b;
-    phi[(int64_t)j * H + h] = a / (1.0f + expf(-a)) * b;
+    if (phi) phi[(int64_t)j * H + h] = a / (1.0f + expf(-a)) * b;
   }
 }
 

@@ -18,7 +18,9 @@
 //       128 gate columns and the same 128 up columns, so every thread has the
 //       a and b of its outputs.
 //   F2  y = phi W_down[e]   [n_e x D] (bf16).
-// Both read the weights in their stored layout (MN-major B operands).
+// Both read the weights in their stored layout (MN-major B operands). F1 over
+// the compacted retained rows (groups from sel_off, phi not written) is the
+// retained-only recompute of [a | b] in the backward.
 //
 // Kernel shape (one CTA per SM, persistent over a device-computed tile list):
 //   warp 0    TMA producer: 128x64 A and 256x64 B tiles, 128-byte swizzle,
@@ -934,7 +936,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             __nv_bfloat16* arow = p.ob0 + j * 2 * p.H;
             uint4* a_dst = reinterpret_cast<uint4*>(arow + h);
             uint4* b_dst = reinterpret_cast<uint4*>(arow + p.H + h);
-            uint4* f_dst = reinterpret_cast<uint4*>(p.ob1 + j * p.H + h);
+            uint4* f_dst = p.ob1 ? reinterpret_cast<uint4*>(p.ob1 + j * p.H + h) : nullptr;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               float a[8], b[8], f[8];
@@ -946,7 +948,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               }
               a_dst[v] = Vec16<__nv_bfloat16>::pack(a);
               b_dst[v] = Vec16<__nv_bfloat16>::pack(b);
-              f_dst[v] = Vec16<__nv_bfloat16>::pack(f);
+              if (f_dst) f_dst[v] = Vec16<__nv_bfloat16>::pack(f);
             }
           }
         }

@@ -27,7 +27,7 @@ EXPORTS = (
     "lrm_expert_fc1_wgrad", "lrm_expert_fc1_dgrad", "lrm_scatter_dx",
     "lrm_dispatch_permute_noalloc", "lrm_selftest_wait_timeout", "lrm_score_variant",
     "lrm_gather_tokens", "lrm_expert_fc1_fwd", "lrm_expert_fc2_fwd", "lrm_combine",
-    "lrm_expert_fwd_grouped",
+    "lrm_expert_fwd_grouped", "lrm_expert_fc1_recompute",
 )
 LRM_METRIC_LRM, LRM_METRIC_GRAD_SQ, LRM_METRIC_GRAD_ABS, LRM_METRIC_RANDOM = range(4)
 LRM_NOALLOC_MAX_CHUNK_ENTRIES = 65536
@@ -77,6 +77,7 @@ def _load():
         "lrm_expert_fc2_fwd": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_combine": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_expert_fwd_grouped": (i32, [sp] + [vp] * 13 + [vp, sz, vp]),
+        "lrm_expert_fc1_recompute": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -270,3 +271,10 @@ def lrm_expert_fwd_grouped(shape, perm, inv, off, alpha, x, w_gate, w_up, w_down
         ctypes.byref(shape), _p(perm), _p(inv), _p(off), _p(alpha), _p(x), _p(w_gate),
         _p(w_up), _p(w_down), _p(x_disp), _p(ab), _p(phi), _p(y), _p(out), _p(ws), ws_bytes,
         _s(stream)))
+
+
+def lrm_expert_fc1_recompute(shape, sel_off, x_c, w_gate, w_up, ab_c, ws, ws_bytes,
+                             stream=None):
+    _check("lrm_expert_fc1_recompute", _lib.lrm_expert_fc1_recompute(
+        ctypes.byref(shape), _p(sel_off), _p(x_c), _p(w_gate), _p(w_up), _p(ab_c), _p(ws),
+        ws_bytes, _s(stream)))

@@ -131,9 +131,15 @@ class RecalibratedExpertBackward:
                              self.sel_off, self.sel_pos, self.ws, self.ws_bytes, stream)
 
     def compact(self, alpha, x, g, ab, phi, stream=None):
+        """Gather the retained rows; ab=None copies no [a | b] (recompute)."""
         lrm.lrm_compact(self.shape, self.perm, self.keep, self.sel_off, self.sel_pos, alpha, x,
-                        g, ab, phi, self.dy_c, self.x_c, self.ab_c, self.phi_c, self.tok_c,
-                        self.row_of_pos, self.ws, self.ws_bytes, stream)
+                        g, ab, phi, self.dy_c, self.x_c, None if ab is None else self.ab_c,
+                        self.phi_c, self.tok_c, self.row_of_pos, self.ws, self.ws_bytes, stream)
+
+    def fc1_recompute(self, w_gate, w_up, stream=None):
+        """[a | b] of the retained rows rebuilt from x_c (no saved [a | b])."""
+        lrm.lrm_expert_fc1_recompute(self.shape, self.sel_off, self.x_c, w_gate, w_up,
+                                     self.ab_c, self.ws, self.ws_bytes, stream)
 
     def score_select_compact(self, alpha, x, g, ab, phi, stream=None, metric: int = 0,
                              seed: int = 0):
@@ -173,13 +179,16 @@ class RecalibratedExpertBackward:
              cap: int = 0, quota: torch.Tensor | None = None, stream=None, metric: int = 0,
              seed: int = 0):
         """One pass of the whole path. ab / phi are in dispatch order; `metric`
-        picks the selection criterion (LRM by default)."""
+        picks the selection criterion (LRM by default). ab=None recomputes
+        [a | b] of the retained rows instead of reading saved state."""
         self.dispatch(topk_idx, stream)
         if quota is None:
             self.quota_from_rate(rate[0], rate[1], cap, stream)
         else:
             self.quota.copy_(quota)
         self.score_select_compact(alpha, x, g, ab, phi, stream, metric, seed)
+        if ab is None:
+            self.fc1_recompute(w_gate, w_up, stream)
         self.expert_bwd(w_gate, w_up, w_down, stream)
 
     def device_error(self, stream=None) -> int:

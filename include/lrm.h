@@ -194,6 +194,8 @@ lrm_status lrm_select_quota(const lrm_shape* shape, const float* score,
  *   phi [N,H] (dispatch order).
  * Outputs (capacity N rows each, first M written): dy_c [N,D], x_c [N,D],
  *   ab_c [N,2H], phi_c [N,H], tok_c [N] int32; row_of_pos [N] int32.
+ * ab and ab_c may both be NULL (then no [a | b] rows are copied; see
+ * lrm_expert_fc1_recompute); one NULL without the other is an error.
  */
 lrm_status lrm_compact(const lrm_shape* shape, const int32_t* perm,
                        const uint8_t* keep, const int32_t* sel_off,
@@ -359,6 +361,20 @@ lrm_status lrm_expert_fwd_grouped(const lrm_shape* shape, const int32_t* perm,
                                   const void* w_down, void* x_disp, void* ab, void* phi,
                                   void* y, float* out, void* ws, size_t ws_bytes,
                                   void* stream);
+
+/*
+ * Retained-only recompute of [a | b] in the backward (RelayMoE Sec. 3.3,
+ * memory-efficient MoE recomputation: the backward rebuilds the expert
+ * intermediates it consumes; LRMoE Sec. 3.1: FC1 and the activation use the
+ * retained identities). ab_c [M,2H] dtype (written, rows of sel_off's
+ * segments) = [x_c W_gate[e] | x_c W_up[e]] from x_c [N,D] (compacted rows,
+ * read) with the layer's FP32 accumulation and one rounding, the same as
+ * lrm_expert_fc1_fwd over the routed rows. With it the saved state needs no
+ * [a | b]: lrm_compact then takes ab = ab_c = NULL and copies none.
+ */
+lrm_status lrm_expert_fc1_recompute(const lrm_shape* shape, const int32_t* sel_off,
+                                    const void* x_c, const void* w_gate, const void* w_up,
+                                    void* ab_c, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

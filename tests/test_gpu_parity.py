@@ -375,3 +375,55 @@ def test_random_criterion_depends_on_seed_only(dev):
         run_gpu(pipe, inp, (1, 2), metric=oracle.METRIC_RANDOM, seed=seed)
         picks.append(pipe.keep[:cfg.N].clone())
     assert torch.equal(picks[0], picks[2]) and not torch.equal(picks[0], picks[1])
+
+
+# ---------------------------------------------------------------------------
+# retained-only recompute of [a | b] (RelayMoE Sec. 3.3)
+# ---------------------------------------------------------------------------
+def recompute_parity(cfg, dev, rate, cap=0):
+    inp_cpu = generate(cfg, device="cpu")
+    inp = _to(inp_cpu, dev)
+    pipe = _pipe(cfg, dev)
+    pipe.dispatch(inp["topk_idx"])
+    phi = pipe.to_dispatch_order(inp["phi_pair"])
+    pipe.ab_c.fill_(float("nan"))  # every retained row must be rebuilt
+    pipe.step(inp["topk_idx"], inp["alpha"], inp["x"], inp["g"], None, phi, inp["w_gate"],
+              inp["w_up"], inp["w_down"], rate=rate, cap=cap)
+    torch.cuda.synchronize()
+    assert pipe.device_error() == 0
+    nin = numpy_inputs(inp_cpu)
+    perm, inv, counts, off = check_dispatch(pipe, nin["topk_idx"], cfg.E)
+    qv = oracle.quota_from_rate(counts, rate[0], rate[1], cap)
+    keep, sel_off, sel_pos = check_selection(pipe, perm, off, qv)
+    M = int(sel_off[-1])
+    ab = oracle.lrm_oracle.permute_rows(nin["ab_pair"], perm)
+    phi_np = oracle.lrm_oracle.permute_rows(nin["phi_pair"], perm)
+    c = oracle.compact(perm, sel_off, sel_pos, nin["alpha"], nin["x"], nin["g"], ab, phi_np,
+                       cfg.K)
+    for name in ("x_c", "phi_c"):
+        assert np.array_equal(to_np(getattr(pipe, name))[:M], c[name]), name
+    c["ab_c"] = oracle.recompute_ab(sel_off, nin["w_gate"], nin["w_up"], c["x_c"])
+    got = to_np(pipe.ab_c)[:M].astype(np.float64)
+    err = np.linalg.norm(got - c["ab_c"], axis=1)
+    assert np.all(err <= 2e-2 * np.linalg.norm(c["ab_c"], axis=1) + 1e-12), "ab_c rows"
+    c["dy_c"] = to_np(pipe.dy_c)[:M].astype(np.float64)
+    return check_backward(pipe, nin, c, sel_off, inv, cfg.T, cfg.K, cfg.dtype)
+
+
+@pytest.mark.parametrize("rate", [(1, 2), (1, 1)])
+def test_recompute_bf16_ragged_tiles(dev, rate):
+    recompute_parity(get_config("qwen3-30b-a3b-t4k", T=1024, D=320, H=192, E=12, K=3), dev,
+                     rate)
+
+
+def test_recompute_fp32(dev):
+    recompute_parity(get_config("tiny", T=200, D=48, H=40, E=6, K=3), dev, (3, 5))
+
+
+def test_recompute_stress_edge_groups(dev):
+    recompute_parity(get_config("stress-e256", T=2048, D=256, H=128), dev, (1, 2), cap=100)
+
+
+def test_recompute_zero_retention(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=256, D=128, H=64, E=8, K=2)
+    recompute_parity(cfg, dev, (0, 1))
