@@ -84,6 +84,12 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-forward", action="store_true",
                     help="skip the separate timing of the forward expert pass")
+    ap.add_argument("--backward", choices=["compacted", "gathered"], default="gathered",
+                    help="compacted: the products read compacted copies of x, [a | b] and "
+                    "phi; gathered: compaction writes only the gradient rows and the "
+                    "products read the others in place")
+    ap.add_argument("--no-other-backward", action="store_true",
+                    help="skip timing the step with the other --backward variant")
     ap.add_argument("--no-recompute", action="store_true",
                     help="skip the timing of the backward step that recomputes [a | b]")
     return ap.parse_args()
@@ -92,8 +98,9 @@ def parse_args():
 # ---------------------------------------------------------------------------
 # algorithmic bytes and flops per launch
 # ---------------------------------------------------------------------------
-def algorithmic(cfg, M: int) -> dict:
-    """Bytes (and flops) each segment must move at minimum, per launch."""
+def algorithmic(cfg, M: int, gathered: bool = False) -> dict:
+    """Bytes (and flops) each segment must move at minimum, per launch
+    (gathered: compaction writes only the gradient rows)."""
     T, D, H, E, K = cfg.T, cfg.D, cfg.H, cfg.E, cfg.K
     N = T * K
     s = 2 if cfg.dtype == "bf16" else 4
@@ -103,7 +110,8 @@ def algorithmic(cfg, M: int) -> dict:
         "quota": {"bytes": 8 * E},
         "score": {"bytes": T * D * s + N * H * s + 4 * N + 4 * N + 4 * N},
         "select": {"bytes": 4 * N + N + 4 * M + 16 * E},
-        "compact": {"bytes": 2 * M * (2 * D + 3 * H) * s + 4 * M * 4 + 5 * N},
+        "compact": {"bytes": (2 * M * D * s if gathered else 2 * M * (2 * D + 3 * H) * s)
+                    + 4 * M * 4 + 5 * N},
         "fc2_dgrad": {"bytes": M * D * s + W + 2 * (M * 2 * H * s), "flops": 2 * M * D * H},
         "fc2_wgrad": {"bytes": M * H * s + M * D * s + E * H * D * 4, "flops": 2 * M * D * H},
         "fc1_wgrad": {"bytes": M * D * s + M * 2 * H * s + 2 * E * D * H * 4,
@@ -264,9 +272,10 @@ def workload_of(args):
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
 
-    from demand_side_expert_gb300 import RecalibratedExpertBackward
+    from demand_side_expert_gb300 import RecalibratedExpertBackward, lrm
     from workloads import generate
 
+    gathered = args.backward == "gathered"
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -295,8 +304,16 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         ev[3].record(stream)
         pipe.select()
         ev[4].record(stream)
-        pipe.compact(inp["alpha"], inp["x"], inp["g"], ab, phi)
+        pipe.compact(inp["alpha"], inp["x"], inp["g"], ab, phi, gathered=gathered)
         ev[5].record(stream)
+        if gathered:  # the products read x, ab and phi rows in place
+            for j, part in enumerate((lrm.LRM_BWD_FC2_DGRAD, lrm.LRM_BWD_FC2_WGRAD,
+                                      lrm.LRM_BWD_FC1_WGRAD, lrm.LRM_BWD_FC1_DGRAD,
+                                      lrm.LRM_BWD_SCATTER_DX)):
+                pipe.expert_bwd_gathered(inp["x"], ab, phi, inp["w_gate"], inp["w_up"],
+                                         inp["w_down"], parts=part)
+                ev[6 + j].record(stream)
+            return
         pipe.fc2_dgrad(inp["w_down"])
         ev[6].record(stream)
         pipe.fc2_wgrad()
@@ -356,12 +373,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     rec = None
     if not args.no_recompute:
         rec = run_recompute(pipe, inp, phi, rate, cfg, flush, stream, args)
+    other = None
+    if not args.no_other_backward:
+        other = run_other_backward(pipe, inp, ab, phi, rate, cfg, flush, stream, args)
 
     if rank != 0:
         return None
 
     peaks = load_peaks()
-    alg = algorithmic(cfg, M)
+    alg = algorithmic(cfg, M, gathered)
     traffic = load_traffic(cfg.name)
     kernels = {}
     for s in SEGMENTS:
@@ -408,6 +428,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "retained_rows": M, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
             "inputs": "resident in HBM",
+            "backward": args.backward,
         },
         "grouped_gemm_pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
         "grouped_gemm_tflops": round(gemm_tflops, 1),
@@ -424,7 +445,40 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line["forward"] = fwd
     if rec is not None:
         line["recompute"] = rec
+    if other is not None:
+        line["other_backward"] = other
     return line, cfg, rate
+
+
+def run_other_backward(pipe, inp, ab, phi, rate, cfg, flush, stream, args):
+    """The whole step again with the other backward variant (compacted copies
+    vs in-place gathers), timed the same way, so both stand side by side."""
+    import torch
+
+    gathered = args.backward != "gathered"
+
+    def step():
+        pipe.step(inp["topk_idx"], inp["alpha"], inp["x"], inp["g"], ab, phi, inp["w_gate"],
+                  inp["w_up"], inp["w_down"], rate=rate, cap=cfg.cap, gathered=gathered)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        flush.fill_(1)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if pipe.device_error() != 0:
+        raise RuntimeError(f"device error word {pipe.device_error()} in the other backward")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return {"backward": "gathered" if gathered else "compacted",
+            "value": round(pipe.retained_rows / (ms * 1e-3), 1), "unit": "rows/s",
+            "ms_per_step": round(ms, 4), "steps": args.steps}
 
 
 def run_recompute(pipe, inp, phi, rate, cfg, flush, stream, args):
@@ -561,7 +615,7 @@ def run_e2e(pipe, inp, ab, phi, rate, cfg, flush, stream, args):
             dev_in[k].copy_(h, non_blocking=True)
         pipe.step(dev_in["topk_idx"], dev_in["alpha"], dev_in["x"], dev_in["g"], dev_in["ab"],
                   dev_in["phi"], inp["w_gate"], inp["w_up"], inp["w_down"], rate=rate,
-                  cap=cfg.cap)
+                  cap=cfg.cap, gathered=args.backward == "gathered")
         host_dx.copy_(pipe.dx, non_blocking=True)
 
     steps = max(1, min(args.steps, 20))

@@ -103,3 +103,28 @@ extern "C" lrm_status lrm_expert_bwd_grouped(
 extern "C" lrm_status lrm_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
   return selftest_wait_timeout(ws, ws_bytes, (cudaStream_t)stream);
 }
+
+extern "C" lrm_status lrm_expert_bwd_gathered(
+    const lrm_shape* s, int32_t parts, const int32_t* sel_off, const int32_t* sel_pos,
+    const int32_t* tok_c, const void* w_gate, const void* w_up, const void* w_down,
+    const void* dy_c, const void* x, const void* ab, const void* phi, const int32_t* inv,
+    const int32_t* row_of_pos, void* dab_c, float* dx_c, float* dw_gate, float* dw_up,
+    float* dw_down, float* dx, void* ws, size_t ws_bytes, void* stream) {
+  lrm_status st = check_common(s, ws, ws_bytes, sel_off);
+  if (st != LRM_OK) return st;
+  if (parts < 0 || parts > LRM_BWD_ALL) return LRM_ERR_INVALID_ARG;
+  if (s->K > 32) return LRM_ERR_UNSUPPORTED;
+  if ((st = check_ptrs(s, {w_gate, w_up, w_down, dw_gate, dw_up, dw_down},
+                       {sel_pos, tok_c, dy_c, x, ab, phi, inv, row_of_pos, dab_c, dx_c, dx})) !=
+      LRM_OK)
+    return st;
+  BwdArgs a{s, sel_off, w_gate, w_up, w_down, dy_c, x, ab, phi, dab_c,
+            dx_c, dw_gate, dw_up, dw_down, error_word(ws), (cudaStream_t)stream};
+  a.sel_pos = sel_pos;
+  a.tok_c = tok_c;
+  const unsigned gemm_parts = (unsigned)parts & kPartAll;
+  if (gemm_parts && (st = run_parts(a, gemm_parts)) != LRM_OK) return st;
+  if (parts & LRM_BWD_SCATTER_DX)
+    return launch_dx_gather(s, dx_c, inv, row_of_pos, dx, error_word(ws), (cudaStream_t)stream);
+  return LRM_OK;
+}

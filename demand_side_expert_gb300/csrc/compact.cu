@@ -57,16 +57,20 @@ compact_kernel(const int32_t* __restrict__ perm, const uint8_t* __restrict__ kee
 #pragma unroll
       for (int u = 0; u < V; ++u) f[u] *= a;
       dyd[c] = Vec16<T>::pack(f);
-      xd[c] = xs[c];
+      if (x_c) xd[c] = xs[c];
     }
-    if (ab) {  // absent when the backward recomputes [a | b] of the retained rows
+    // the saved-state copies are skipped when their destination is absent:
+    // [a | b] recomputed, or rows gathered by the products themselves
+    if (ab_c) {
       const uint4* abs_ = reinterpret_cast<const uint4*>(ab + (int64_t)i * 2 * H);
       uint4* abd = reinterpret_cast<uint4*>(ab_c + j * 2 * H);
       for (int c = lane; c < abv; c += 32) abd[c] = ld_stream(abs_ + c);
     }
-    const uint4* ps = reinterpret_cast<const uint4*>(phi + (int64_t)i * H);
-    uint4* pd = reinterpret_cast<uint4*>(phi_c + j * H);
-    for (int c = lane; c < hv; c += 32) pd[c] = ld_stream(ps + c);
+    if (phi_c) {
+      const uint4* ps = reinterpret_cast<const uint4*>(phi + (int64_t)i * H);
+      uint4* pd = reinterpret_cast<uint4*>(phi_c + j * H);
+      for (int c = lane; c < hv; c += 32) pd[c] = ld_stream(ps + c);
+    }
     if (lane == 0) {
       tok_c[j] = (int32_t)t;
       row_of_pos[i] = (int32_t)j;
@@ -140,11 +144,11 @@ extern "C" lrm_status lrm_compact(const lrm_shape* s, const int32_t* perm,
   if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
   const int64_t N = (int64_t)s->T * s->K;
   if (N == 0) return LRM_OK;
-  const void* ptrs[] = {perm, keep, sel_off, sel_pos, alpha, x, g, phi,
-                        dy_c, x_c, phi_c, tok_c, row_of_pos};
+  const void* ptrs[] = {perm, keep, sel_off, sel_pos, alpha, g, dy_c, tok_c, row_of_pos};
   for (const void* p : ptrs)
     if (!p) return LRM_ERR_INVALID_ARG;
-  if ((ab == nullptr) != (ab_c == nullptr)) return LRM_ERR_INVALID_ARG;
+  // a copied row needs its source; absent destinations are skipped
+  if ((x_c && !x) || (ab_c && !ab) || (phi_c && !phi)) return LRM_ERR_INVALID_ARG;
   const void* vec[] = {x, g, ab, phi, dy_c, x_c, ab_c, phi_c};
   for (const void* p : vec)
     if (!aligned16(p)) return LRM_ERR_UNSUPPORTED;

@@ -25,9 +25,12 @@ __device__ __forceinline__ int expert_of_row(const int32_t* sel_off, int E, int 
 }
 
 // G1 + SwiGLU gradient: dab_c[j] = [da | db]
+// ab_rows (optional): the row of ab_c (then the uncompacted saved state)
+// read for compacted row j.
 __global__ void f32_g1_kernel(const int32_t* __restrict__ sel_off, int E, int D, int H,
                               const float* __restrict__ dy_c, const float* __restrict__ w_down,
-                              const float* __restrict__ ab_c, float* __restrict__ dab_c) {
+                              const float* __restrict__ ab_c, const int32_t* __restrict__ ab_rows,
+                              float* __restrict__ dab_c) {
   const int64_t M = sel_off[E];
   for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < M * H;
        o += (int64_t)gridDim.x * blockDim.x) {
@@ -37,8 +40,9 @@ __global__ void f32_g1_kernel(const int32_t* __restrict__ sel_off, int E, int D,
     const float* dy = dy_c + (int64_t)j * D;
     float dphi = 0.f;
     for (int d = 0; d < D; ++d) dphi = fmaf(dy[d], wd[d], dphi);
-    const float a = ab_c[(int64_t)j * 2 * H + h];
-    const float b = ab_c[(int64_t)j * 2 * H + H + h];
+    const int64_t r = ab_rows ? ab_rows[j] : j;
+    const float a = ab_c[r * 2 * H + h];
+    const float b = ab_c[r * 2 * H + H + h];
     const float s = 1.0f / (1.0f + expf(-a));
     dab_c[(int64_t)j * 2 * H + h] = dphi * b * s * (1.0f + a * (1.0f - s));
     dab_c[(int64_t)j * 2 * H + H + h] = dphi * a * s;
@@ -66,8 +70,8 @@ __global__ void f32_g4_kernel(const int32_t* __restrict__ sel_off, int E, int D,
 
 // G2: dW_down[e][h, d] = sum_{j in e} phi_c[j,h] dy_c[j,d]
 __global__ void f32_g2_kernel(const int32_t* __restrict__ sel_off, int E, int D, int H,
-                              const float* __restrict__ phi_c, const float* __restrict__ dy_c,
-                              float* __restrict__ dw_down) {
+                              const float* __restrict__ phi_c, const int32_t* __restrict__ rows,
+                              const float* __restrict__ dy_c, float* __restrict__ dw_down) {
   const int64_t total = (int64_t)E * H * D;
   for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total;
        o += (int64_t)gridDim.x * blockDim.x) {
@@ -75,15 +79,16 @@ __global__ void f32_g2_kernel(const int32_t* __restrict__ sel_off, int E, int D,
     const int h = (int)((o / D) % H), d = (int)(o % D);
     float acc = 0.f;
     for (int j = sel_off[e]; j < sel_off[e + 1]; ++j)
-      acc = fmaf(phi_c[(int64_t)j * H + h], dy_c[(int64_t)j * D + d], acc);
+      acc = fmaf(phi_c[(rows ? (int64_t)rows[j] : j) * H + h], dy_c[(int64_t)j * D + d], acc);
     dw_down[o] = acc;
   }
 }
 
 // G3: dW_gate[e][d, n] / dW_up[e][d, n - H] = sum_{j in e} x_c[j,d] dab_c[j,n]
 __global__ void f32_g3_kernel(const int32_t* __restrict__ sel_off, int E, int D, int H,
-                              const float* __restrict__ x_c, const float* __restrict__ dab_c,
-                              float* __restrict__ dw_gate, float* __restrict__ dw_up) {
+                              const float* __restrict__ x_c, const int32_t* __restrict__ rows,
+                              const float* __restrict__ dab_c, float* __restrict__ dw_gate,
+                              float* __restrict__ dw_up) {
   const int64_t total = (int64_t)E * D * 2 * H;
   for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total;
        o += (int64_t)gridDim.x * blockDim.x) {
@@ -91,7 +96,7 @@ __global__ void f32_g3_kernel(const int32_t* __restrict__ sel_off, int E, int D,
     const int d = (int)((o / (2 * H)) % D), n = (int)(o % (2 * H));
     float acc = 0.f;
     for (int j = sel_off[e]; j < sel_off[e + 1]; ++j)
-      acc = fmaf(x_c[(int64_t)j * D + d], dab_c[(int64_t)j * 2 * H + n], acc);
+      acc = fmaf(x_c[(rows ? (int64_t)rows[j] : j) * D + d], dab_c[(int64_t)j * 2 * H + n], acc);
     float* out = n < H ? dw_gate : dw_up;
     out[((int64_t)e * D + d) * H + (n < H ? n : n - H)] = acc;
   }
@@ -173,13 +178,15 @@ lrm_status launch_bwd_f32(const BwdArgs& a, unsigned parts) {
   if (parts & kPartFc2Dgrad)
     f32_g1_kernel<<<grid(N * H), kF32Threads, 0, cs>>>(a.sel_off, E, D, H, dy,
                                                        (const float*)a.w_down,
-                                                       (const float*)a.ab_c, (float*)a.dab_c);
+                                                       (const float*)a.ab_c, a.sel_pos,
+                                                       (float*)a.dab_c);
   if (parts & kPartFc2Wgrad)
     f32_g2_kernel<<<grid((int64_t)E * H * D), kF32Threads, 0, cs>>>(
-        a.sel_off, E, D, H, (const float*)a.phi_c, dy, a.dw_down);
+        a.sel_off, E, D, H, (const float*)a.phi_c, a.sel_pos, dy, a.dw_down);
   if (parts & kPartFc1Wgrad)
     f32_g3_kernel<<<grid((int64_t)E * D * 2 * H), kF32Threads, 0, cs>>>(
-        a.sel_off, E, D, H, (const float*)a.x_c, (const float*)a.dab_c, a.dw_gate, a.dw_up);
+        a.sel_off, E, D, H, (const float*)a.x_c, a.tok_c, (const float*)a.dab_c, a.dw_gate,
+        a.dw_up);
   if (parts & kPartFc1Dgrad)
     f32_g4_kernel<<<grid(N * D), kF32Threads, 0, cs>>>(a.sel_off, E, D, H,
                                                        (const float*)a.dab_c,

@@ -35,6 +35,10 @@
 //             32-column chunk ahead); FP32 outputs go through a per-warp
 //             32x32 swizzled shared-memory block and a TMA bulk-tensor store,
 //             so every 128-byte line is written whole.
+//   warps 10-13 (weight-gradient products on single CTAs only): when the A
+//             rows are read in place by index (phi rows by dispatch position,
+//             x rows by token) instead of from compacted copies, these warps
+//             gather them with 16-byte async copies into the swizzled layout.
 // Data-gradient tiles are cut at group ends (rows past m_e are computed and
 // masked on store). Weight-gradient tiles reduce over [sel_off[e],
 // sel_off[e+1]) in 64-row blocks; rows of the last block that belong to the
@@ -57,6 +61,7 @@ constexpr int BM = 128, BN = 256, BK = 64;  // rows per CTA, accumulator columns
 constexpr int MAX_STAGES = 6;  // operand ring depth (runtime: as deep as shared memory allows)
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kGatherWarps = 4;  // weight-gradient products: A rows gathered by index
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 // B rows a CTA loads: all BN columns alone, half of them in a CTA pair
 template <bool PAIR>
@@ -93,6 +98,14 @@ struct Params {
   float* out1;
   __nv_bfloat16* ob0;  // F1: ab, F2: y
   __nv_bfloat16* ob1;  // F1: phi
+  // gathered operands (null: compacted rows): G1 reads the saved [a | b] row
+  // ab_rows[j] of compacted row j; G2 / G3 read their A operand (phi / x)
+  // row a_rows[j] of a_src [a_src_rows, a_src_cols] with 16-byte async copies
+  const int32_t* ab_rows;
+  const int32_t* a_rows;
+  const __nv_bfloat16* a_src;
+  int a_src_rows, a_src_cols;
+  int ab_src_rows;  // rows of the [a | b] source (bound for ab_rows)
   int32_t* err;
 };
 
@@ -184,6 +197,21 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
       : "memory");
+}
+// 16-byte asynchronous copy global -> shared (zero-filled when !valid), and
+// an arrival on an mbarrier once all of this thread's earlier copies landed
+// (counted as one of the barrier's expected arrivals)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(su32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y, int z) {
@@ -381,6 +409,14 @@ struct Geo {
   static constexpr bool kBmn = kWgrad || kFwd;  // B operand MN-major
 };
 
+// Threads of one CTA: copy warp, MMA warp, epilogue warps, and for the
+// single-CTA weight-gradient products the warps that gather A rows
+template <int MODE, bool PAIR>
+struct Threads {
+  static constexpr int kGather = (Geo<MODE>::kWgrad && !PAIR) ? kGatherWarps : 0;
+  static constexpr int kCount = kThreads + 32 * kGather;
+};
+
 // ----------------------------------------------------------------------------
 // tile list
 // ----------------------------------------------------------------------------
@@ -492,8 +528,10 @@ __device__ __forceinline__ void swiglu_chunk(const uint32_t (&r)[32], const uint
 //   odd CTA's copy lands on its own full barrier, its (otherwise idle) MMA warp
 //   zeroes the rows past the group end and then arrives on the even CTA's.
 template <int MODE, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Threads<MODE, PAIR>::kCount, 1)
 grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
+  constexpr int NT = Threads<MODE, PAIR>::kCount;
+  constexpr int NG = Threads<MODE, PAIR>::kGather;
   constexpr bool WG = Geo<MODE>::kWgrad;
   constexpr int BNL = Cfg<PAIR>::kBRows;
   constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
@@ -533,7 +571,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     *bad_flag = 0;
   }
   __syncthreads();
-  for (int i = tid; i <= E; i += kThreads) {
+  for (int i = tid; i <= E; i += NT) {
     const int v = p.sel_off[i];
     const int prev = i > 0 ? p.sel_off[i - 1] : 0;
     goff[i] = v;
@@ -541,7 +579,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   }
   __syncthreads();
   if (*bad_flag) {
-    for (int i = tid; i <= E; i += kThreads) goff[i] = 0;
+    for (int i = tid; i <= E; i += NT) goff[i] = 0;
     if (tid == 0) flag_error(p.err, LRM_DEVERR_INDEX);
   }
   __syncthreads();
@@ -571,7 +609,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   }
   if constexpr (WG) {
     // experts ordered by retained rows (descending, then by id): longest first
-    for (int e = tid; e < E; e += kThreads) {
+    for (int e = tid; e < E; e += NT) {
       const int m = goff[e + 1] - goff[e];
       int rank_e = 0;
       for (int f = 0; f < E; ++f) {
@@ -602,8 +640,11 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     sc.tpre = tab;
   }
   if (tid == 0) {
+    // full: the copy warp's arrival (two in a pair's even CTA), plus one per
+    // lane of the copy warp when it gathers A rows with async copies
+    const uint32_t full_count = (PAIR && leader) ? 2u : (NG > 0 && p.a_rows) ? 33u : 1u;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], PAIR && leader ? 2 : 1);
+      mbar_init(&full[s], full_count);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -670,8 +711,10 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           // odd CTA, ordinary block) the even CTA's
           const bool to_leader = PAIR && !leader && !tailz;
           const uint32_t bar_cl = to_leader ? mapa(&full[stage], 0) : 0u;
+          const bool gathered_a = NG > 0 && p.a_rows != nullptr;  // A copied by the gather warps
           if (!to_leader)
-            mbar_expect_tx(&full[stage], (PAIR && leader && !tailz) ? 2 * STB : STB);
+            mbar_expect_tx(&full[stage], gathered_a ? STB - A_BYTES
+                                         : (PAIR && leader && !tailz) ? 2 * STB : STB);
           auto load2 = [&](uint8_t* dst, const CUtensorMap* m, int x, int y) {
             if (to_leader) tma_load_2d_pair(dst, m, bar_cl, x, y);
             else tma_load_2d(dst, m, &full[stage], x, y);
@@ -706,8 +749,11 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               load3(b_s + i * BOX_BYTES, mapB, nb0 + 64 * i, kb * BK, t.e);
           } else {
             const int y = t.row0 + kb * BK;
+            if (!gathered_a) {
 #pragma unroll
-            for (int i = 0; i < BM / 64; ++i) load2(a_s + i * BOX_BYTES, mapA, t.cm0 + 64 * i, y);
+              for (int i = 0; i < BM / 64; ++i)
+                load2(a_s + i * BOX_BYTES, mapA, t.cm0 + 64 * i, y);
+            }
 #pragma unroll
             for (int i = 0; i < BNL / 64; ++i) load2(b_s + i * BOX_BYTES, mapB, nb0 + 64 * i, y);
           }
@@ -755,6 +801,8 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const int valid = (WG && kb == t.nkb - 1) ? t.valid : BK;
         const int nks = (valid + 15) >> 4;
         if constexpr (WG) {
+          // rows written by async copies (generic proxy) before the MMA reads them
+          if (NG > 0 && p.a_rows) fence_async_smem();
           if (valid & 15) zero_tail(a_s, valid);
         }
         tc_fence_after();
@@ -822,6 +870,67 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
       }
     }
+  } else if (warp >= 2 + kEpiWarps) {
+    // ===================== A-row gather warps =====================
+    // Weight-gradient products whose A rows are read by index: gather warp g
+    // fills the A tile of every ng-th K block (g, g + ng, ...), so each warp
+    // has ng ring periods to hide the latency of its index loads. ng never
+    // exceeds the ring depth: a warp's previous K block is then at most one
+    // ring lap behind, so the slot it waits for is at most one phase behind
+    // and the parity wait cannot mistake an older phase for the one it needs
+    // (with more warps than stages a warp could run two laps ahead). For one K
+    // block: lane l fetches the row indices of K-block rows l and l + 32
+    // before the ring slot frees; then each instruction copies four whole
+    // 128-byte rows of an A box (lane l: row 4i + l/8, 16-byte chunk l%8,
+    // placed at its 128-byte swizzle position), and each lane arrives on the
+    // stage's full barrier once its copies have landed (32 of its 33
+    // arrivals; the copy warp arms it for the B tile). Rows past the group
+    // end repeat its last row (the MMA warp zeroes or skips them); rows or
+    // columns outside the source are zero-filled.
+    if constexpr (NG > 0) {
+      const int ng = min(NG, STAGES);
+      const int g = warp - (2 + kEpiWarps);
+      if (p.a_rows && !p.selftest && g < ng) {
+        const int chunk = lane & 7;
+        const size_t row_bytes = (size_t)p.a_src_cols * 2;
+        const char* src_base = reinterpret_cast<const char*>(p.a_src);
+        uint32_t it = 0;  // K blocks of this CTA so far
+        bool stop = false;
+        for (int tau = unit; tau < sc.total && !stop; tau += units) {
+          const Tile t = decode<MODE>(sc, tau, rank);
+          const int gend = t.row0 + (t.nkb - 1) * BK + t.valid;  // group end
+          for (int kb = 0; kb < t.nkb; ++kb, ++it) {
+            if ((int)(it % (uint32_t)ng) != g) continue;
+            const uint32_t stage = it % (uint32_t)STAGES;
+            const uint32_t phase = (it / (uint32_t)STAGES) & 1u;
+            const int y = t.row0 + kb * BK;
+            const int ia = p.a_rows[min(y + lane, gend - 1)];
+            const int ib = p.a_rows[min(y + lane + 32, gend - 1)];
+            if (!warp_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_ns)) {
+              stop = true;
+              break;
+            }
+            uint8_t* a_s = stages + stage * STB;
+#pragma unroll 4
+            for (int i = 0; i < BK / 4; ++i) {
+              const int r = 4 * i + (lane >> 3);  // row of the K block
+              const int src = __shfl_sync(0xffffffffu, i < BK / 8 ? ia : ib, r & 31);
+              const bool row_ok = src >= 0 && src < p.a_src_rows;
+#pragma unroll
+              for (int box = 0; box < BM / 64; ++box) {
+                const int col = t.cm0 + 64 * box + 8 * chunk;
+                const bool ok = row_ok && col < p.a_src_cols;
+                const char* gp = ok ? src_base + (size_t)src * row_bytes + (size_t)col * 2
+                                    : src_base;
+                cp_async16(a_s + box * BOX_BYTES + r * 128 + ((chunk ^ (r & 7)) << 4), gp, ok);
+              }
+            }
+            cp_async_arrive(&full[stage]);
+          }
+        }
+        cp_async_wait_all();
+      }
+    }
   } else {
     // ===================== epilogue (warps 2..9) =====================
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -880,9 +989,17 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if constexpr (MODE == kG1) {
-        const bool rv = row_local < t.cvalid;
+        bool rv = row_local < t.cvalid;
         const int64_t j = (int64_t)t.cm0 + row_local;
-        const __nv_bfloat16* arow = p.ab_c + j * 2 * p.H;
+        int64_t src = j;  // row of the saved [a | b]
+        if (p.ab_rows && rv) {
+          src = p.ab_rows[j];
+          if (src < 0 || src >= p.ab_src_rows) {
+            flag_error(p.err, LRM_DEVERR_INDEX);
+            rv = false;
+          }
+        }
+        const __nv_bfloat16* arow = p.ab_c + src * 2 * p.H;
         __nv_bfloat16* drow = p.dab_c + j * 2 * p.H;
         uint4 a_cur[4], b_cur[4], a_nxt[4], b_nxt[4];
         auto load_ab = [&](int h, uint4 (&av)[4], uint4 (&bv)[4]) {
@@ -1087,7 +1204,7 @@ static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStr
   const int64_t units = std::max<int64_t>(1, std::min<int64_t>(tiles, sms / per_unit));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units * per_unit), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Threads<MODE, PAIR>::kCount, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = cs;
   cudaLaunchAttribute attr[1];
@@ -1121,6 +1238,15 @@ static lrm_status launch_any(const Maps& single, const Maps& pair, const Params&
     return launch_mode<MODE, false>(single, p, tiles_single, cs);
 }
 
+// Weight-gradient products with gathered A rows run on single CTAs (the
+// gather producer is written for one CTA per tile).
+template <int MODE>
+static lrm_status launch_gather_or_any(const Maps& m, const Params& p, int64_t tiles_single,
+                                       int64_t tiles_pair, cudaStream_t cs) {
+  if (p.a_rows) return launch_mode<MODE, false>(m, p, tiles_single, cs);
+  return launch_any<MODE>(m, m, p, tiles_single, tiles_pair, cs);
+}
+
 }  // namespace tc
 
 lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
@@ -1147,8 +1273,16 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   p.out1 = nullptr;
   p.ob0 = nullptr;
   p.ob1 = nullptr;
+  p.ab_rows = nullptr;
+  p.a_rows = nullptr;
+  p.a_src = nullptr;
+  p.a_src_rows = p.a_src_cols = 0;
+  p.ab_src_rows = (int)N;
   p.err = a.err;
   lrm_status st = LRM_OK;
+  const bool gathered = a.sel_pos != nullptr;
+  if (gathered && !a.tok_c) return LRM_ERR_INVALID_ARG;
+  const uint64_t tok_rows = std::max<uint64_t>(s->T, 1);
   // upper bounds of the tile counts (the exact ones depend on device-side sizes)
   auto dg_tiles = [&](int tm, int ncols) {
     return ((int64_t)N / tm + E) * ((ncols + BN - 1) / BN);
@@ -1169,9 +1303,11 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     m2.a = m1.a;
     m1.b2 = m1.o1 = m1.o2 = m1.b;
     m2.b2 = m2.o1 = m2.o2 = m2.b;
+    p.ab_rows = gathered ? a.sel_pos : nullptr;
     if ((st = launch_any<kG1>(m1, m2, p, dg_tiles(BM, H), dg_tiles(2 * BM, H), a.stream)) !=
         LRM_OK)
       return st;
+    p.ab_rows = nullptr;
   }
   if (parts & kPartFc2Wgrad) {
     Maps m;
@@ -1182,13 +1318,18 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     m.b2 = m.b;
     m.o2 = m.o1;
     p.out0 = a.dw_down;
-    if ((st = launch_any<kG2>(m, m, p, wg_tiles(BM, H, D), wg_tiles(2 * BM, H, D), a.stream)) !=
-        LRM_OK)
+    p.a_rows = gathered ? a.sel_pos : nullptr;
+    p.a_src = reinterpret_cast<const __nv_bfloat16*>(a.phi_c);
+    p.a_src_rows = (int)N;
+    p.a_src_cols = H;
+    if ((st = launch_gather_or_any<kG2>(m, p, wg_tiles(BM, H, D), wg_tiles(2 * BM, H, D),
+                                        a.stream)) != LRM_OK)
       return st;
+    p.a_rows = nullptr;
   }
   if (parts & kPartFc1Wgrad) {
     Maps m;
-    if (!make_map(&m.a, a.x_c, false, 2, 1, rows, D, 64, 64) ||
+    if (!make_map(&m.a, a.x_c, false, 2, 1, gathered ? tok_rows : rows, D, 64, 64) ||
         !make_map(&m.b, a.dab_c, false, 2, 1, rows, 2 * H, 64, 64) ||
         !make_map(&m.o1, a.dw_gate, true, 3, E, D, H, 32, 32) ||
         !make_map(&m.o2, a.dw_up, true, 3, E, D, H, 32, 32))
@@ -1196,9 +1337,14 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     m.b2 = m.b;
     p.out0 = a.dw_gate;
     p.out1 = a.dw_up;
-    if ((st = launch_any<kG3>(m, m, p, wg_tiles(BM, D, 2 * H), wg_tiles(2 * BM, D, 2 * H),
-                              a.stream)) != LRM_OK)
+    p.a_rows = gathered ? a.tok_c : nullptr;
+    p.a_src = reinterpret_cast<const __nv_bfloat16*>(a.x_c);
+    p.a_src_rows = s->T;
+    p.a_src_cols = D;
+    if ((st = launch_gather_or_any<kG3>(m, p, wg_tiles(BM, D, 2 * H), wg_tiles(2 * BM, D, 2 * H),
+                                        a.stream)) != LRM_OK)
       return st;
+    p.a_rows = nullptr;
   }
   if (parts & kPartFc1Dgrad) {
     Maps m1, m2;

@@ -16,6 +16,11 @@ struct BwdArgs {
   float *dx_c, *dw_gate, *dw_up, *dw_down;
   int32_t* err;
   cudaStream_t stream;
+  // Gathered operands: when set, ab_c / phi_c hold the uncompacted saved
+  // state [N rows, dispatch order] read at row sel_pos[j], and x_c the token
+  // rows [T rows] read at row tok_c[j], for compacted row j.
+  const int32_t* sel_pos = nullptr;
+  const int32_t* tok_c = nullptr;
 };
 
 // Sub-steps of the expert backward, in dependency order.

@@ -27,8 +27,10 @@ EXPORTS = (
     "lrm_expert_fc1_wgrad", "lrm_expert_fc1_dgrad", "lrm_scatter_dx",
     "lrm_dispatch_permute_noalloc", "lrm_selftest_wait_timeout", "lrm_score_variant",
     "lrm_gather_tokens", "lrm_expert_fc1_fwd", "lrm_expert_fc2_fwd", "lrm_combine",
-    "lrm_expert_fwd_grouped", "lrm_expert_fc1_recompute",
+    "lrm_expert_fwd_grouped", "lrm_expert_fc1_recompute", "lrm_expert_bwd_gathered",
 )
+LRM_BWD_FC2_DGRAD, LRM_BWD_FC2_WGRAD, LRM_BWD_FC1_WGRAD = 1, 2, 4
+LRM_BWD_FC1_DGRAD, LRM_BWD_SCATTER_DX, LRM_BWD_ALL = 8, 16, 31
 LRM_METRIC_LRM, LRM_METRIC_GRAD_SQ, LRM_METRIC_GRAD_ABS, LRM_METRIC_RANDOM = range(4)
 LRM_NOALLOC_MAX_CHUNK_ENTRIES = 65536
 
@@ -78,6 +80,7 @@ def _load():
         "lrm_combine": (i32, [sp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_expert_fwd_grouped": (i32, [sp] + [vp] * 13 + [vp, sz, vp]),
         "lrm_expert_fc1_recompute": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "lrm_expert_bwd_gathered": (i32, [sp, i32] + [vp] * 18 + [vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -278,3 +281,12 @@ def lrm_expert_fc1_recompute(shape, sel_off, x_c, w_gate, w_up, ab_c, ws, ws_byt
     _check("lrm_expert_fc1_recompute", _lib.lrm_expert_fc1_recompute(
         ctypes.byref(shape), _p(sel_off), _p(x_c), _p(w_gate), _p(w_up), _p(ab_c), _p(ws),
         ws_bytes, _s(stream)))
+
+
+def lrm_expert_bwd_gathered(shape, parts, sel_off, sel_pos, tok_c, w_gate, w_up, w_down, dy_c,
+                            x, ab, phi, inv, row_of_pos, dab_c, dx_c, dw_gate, dw_up, dw_down,
+                            dx, ws, ws_bytes, stream=None):
+    _check("lrm_expert_bwd_gathered", _lib.lrm_expert_bwd_gathered(
+        ctypes.byref(shape), parts, _p(sel_off), _p(sel_pos), _p(tok_c), _p(w_gate), _p(w_up),
+        _p(w_down), _p(dy_c), _p(x), _p(ab), _p(phi), _p(inv), _p(row_of_pos), _p(dab_c),
+        _p(dx_c), _p(dw_gate), _p(dw_up), _p(dw_down), _p(dx), _p(ws), ws_bytes, _s(stream)))

@@ -130,11 +130,16 @@ class RecalibratedExpertBackward:
         lrm.lrm_select_quota(self.shape, self.score, self.off, self.quota, self.keep,
                              self.sel_off, self.sel_pos, self.ws, self.ws_bytes, stream)
 
-    def compact(self, alpha, x, g, ab, phi, stream=None):
-        """Gather the retained rows; ab=None copies no [a | b] (recompute)."""
+    def compact(self, alpha, x, g, ab, phi, stream=None, gathered: bool = False):
+        """Gather the retained rows; ab=None copies no [a | b] (recompute);
+        gathered=True writes only the gradient rows (the products then read
+        x, ab and phi in place)."""
+        x_c = None if gathered else self.x_c
+        ab_c = None if (gathered or ab is None) else self.ab_c
+        phi_c = None if gathered else self.phi_c
         lrm.lrm_compact(self.shape, self.perm, self.keep, self.sel_off, self.sel_pos, alpha, x,
-                        g, ab, phi, self.dy_c, self.x_c, None if ab is None else self.ab_c,
-                        self.phi_c, self.tok_c, self.row_of_pos, self.ws, self.ws_bytes, stream)
+                        g, ab, phi, self.dy_c, x_c, ab_c, phi_c, self.tok_c, self.row_of_pos,
+                        self.ws, self.ws_bytes, stream)
 
     def fc1_recompute(self, w_gate, w_up, stream=None):
         """[a | b] of the retained rows rebuilt from x_c (no saved [a | b])."""
@@ -142,10 +147,20 @@ class RecalibratedExpertBackward:
                                      self.ab_c, self.ws, self.ws_bytes, stream)
 
     def score_select_compact(self, alpha, x, g, ab, phi, stream=None, metric: int = 0,
-                             seed: int = 0):
+                             seed: int = 0, gathered: bool = False):
         self.score_pairs(alpha, g, phi, stream, metric, seed)
         self.select(stream)
-        self.compact(alpha, x, g, ab, phi, stream)
+        self.compact(alpha, x, g, ab, phi, stream, gathered)
+
+    def expert_bwd_gathered(self, x, ab, phi, w_gate, w_up, w_down, parts: int | None = None,
+                            stream=None):
+        """The expert backward reading x, ab and phi rows in place (after a
+        gathered compaction); `parts` selects sub-steps (lrm.LRM_BWD_*)."""
+        lrm.lrm_expert_bwd_gathered(
+            self.shape, lrm.LRM_BWD_ALL if parts is None else parts, self.sel_off, self.sel_pos,
+            self.tok_c, w_gate, w_up, w_down, self.dy_c, x, ab, phi, self.inv, self.row_of_pos,
+            self.dab_c, self.dx_c, self.dw_gate, self.dw_up, self.dw_down, self.dx, self.ws,
+            self.ws_bytes, stream)
 
     def expert_bwd(self, w_gate, w_up, w_down, stream=None):
         lrm.lrm_expert_bwd_grouped(
@@ -177,16 +192,22 @@ class RecalibratedExpertBackward:
 
     def step(self, topk_idx, alpha, x, g, ab, phi, w_gate, w_up, w_down, rate=(1, 1),
              cap: int = 0, quota: torch.Tensor | None = None, stream=None, metric: int = 0,
-             seed: int = 0):
+             seed: int = 0, gathered: bool = False):
         """One pass of the whole path. ab / phi are in dispatch order; `metric`
         picks the selection criterion (LRM by default). ab=None recomputes
-        [a | b] of the retained rows instead of reading saved state."""
+        [a | b] of the retained rows instead of reading saved state;
+        gathered=True lets the products read x, ab and phi rows in place."""
+        if gathered and ab is None:
+            raise ValueError("the gathered backward reads saved [a | b]")
         self.dispatch(topk_idx, stream)
         if quota is None:
             self.quota_from_rate(rate[0], rate[1], cap, stream)
         else:
             self.quota.copy_(quota)
-        self.score_select_compact(alpha, x, g, ab, phi, stream, metric, seed)
+        self.score_select_compact(alpha, x, g, ab, phi, stream, metric, seed, gathered)
+        if gathered:
+            self.expert_bwd_gathered(x, ab, phi, w_gate, w_up, w_down, stream=stream)
+            return
         if ab is None:
             self.fc1_recompute(w_gate, w_up, stream)
         self.expert_bwd(w_gate, w_up, w_down, stream)

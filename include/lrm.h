@@ -194,8 +194,10 @@ lrm_status lrm_select_quota(const lrm_shape* shape, const float* score,
  *   phi [N,H] (dispatch order).
  * Outputs (capacity N rows each, first M written): dy_c [N,D], x_c [N,D],
  *   ab_c [N,2H], phi_c [N,H], tok_c [N] int32; row_of_pos [N] int32.
- * ab and ab_c may both be NULL (then no [a | b] rows are copied; see
- * lrm_expert_fc1_recompute); one NULL without the other is an error.
+ * x_c, ab_c and phi_c may each be NULL: that copy is skipped and its source
+ * may be NULL too (see lrm_expert_fc1_recompute, which rebuilds [a | b], and
+ * lrm_expert_bwd_gathered, which reads x, ab and phi rows in place). A
+ * non-NULL destination with a NULL source is an error.
  */
 lrm_status lrm_compact(const lrm_shape* shape, const int32_t* perm,
                        const uint8_t* keep, const int32_t* sel_off,
@@ -375,6 +377,43 @@ lrm_status lrm_expert_fwd_grouped(const lrm_shape* shape, const int32_t* perm,
 lrm_status lrm_expert_fc1_recompute(const lrm_shape* shape, const int32_t* sel_off,
                                     const void* x_c, const void* w_gate, const void* w_up,
                                     void* ab_c, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The expert backward with its row operands read in place instead of from
+ * compacted copies. LRMoE Sec. 3.1 (compact runtime) asks that the products
+ * run over the retained rows only, in a consistent pair order, with no
+ * zero-masked rows; here the compaction writes only the gradient rows
+ * dy_c = alpha * g (lrm_compact with x_c = ab_c = phi_c = NULL) and the
+ * products gather the rest by index:
+ *   FC2 dgrad + SwiGLU grad  reads [a | b] row sel_pos[j] of ab  [N,2H];
+ *   FC2 wgrad                reads phi row sel_pos[j] of phi     [N,H];
+ *   FC1 wgrad                reads x row tok_c[j] of x           [T,D];
+ * (j = compacted row; ab and phi in dispatch order as lrm_score reads them).
+ * The FC1 dgrad product and the dx scatter are those of
+ * lrm_expert_bwd_grouped. The results equal the compacted form's bit for
+ * bit: the same tiles and reduction order, only the operand source differs.
+ * parts: an OR of LRM_BWD_* selecting the sub-steps to run, in this order.
+ * Other arguments as lrm_expert_bwd_grouped. Row indices outside their
+ * source are read as zero rows (FC2 / FC1 wgrad) or skipped and flagged
+ * LRM_DEVERR_INDEX (FC2 dgrad).
+ */
+enum {
+  LRM_BWD_FC2_DGRAD = 1,
+  LRM_BWD_FC2_WGRAD = 2,
+  LRM_BWD_FC1_WGRAD = 4,
+  LRM_BWD_FC1_DGRAD = 8,
+  LRM_BWD_SCATTER_DX = 16,
+  LRM_BWD_ALL = 31
+};
+lrm_status lrm_expert_bwd_gathered(const lrm_shape* shape, int32_t parts,
+                                   const int32_t* sel_off, const int32_t* sel_pos,
+                                   const int32_t* tok_c, const void* w_gate,
+                                   const void* w_up, const void* w_down, const void* dy_c,
+                                   const void* x, const void* ab, const void* phi,
+                                   const int32_t* inv, const int32_t* row_of_pos,
+                                   void* dab_c, float* dx_c, float* dw_gate, float* dw_up,
+                                   float* dw_down, float* dx, void* ws, size_t ws_bytes,
+                                   void* stream);
 
 #ifdef __cplusplus
 }

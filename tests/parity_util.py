@@ -37,14 +37,14 @@ def rel_fro(a, b) -> float:
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a))
 
 
-def run_gpu(pipe, inp: dict, rate=(1, 1), cap=0, quota=None, metric=0, seed=0):
+def run_gpu(pipe, inp: dict, rate=(1, 1), cap=0, quota=None, metric=0, seed=0, gathered=False):
     """Dispatch, lay out the saved state, run the whole path. Returns (ab, phi)."""
     pipe.dispatch(inp["topk_idx"])
     ab = pipe.to_dispatch_order(inp["ab_pair"])
     phi = pipe.to_dispatch_order(inp["phi_pair"])
     pipe.step(inp["topk_idx"], inp["alpha"], inp["x"], inp["g"], ab, phi, inp["w_gate"],
               inp["w_up"], inp["w_down"], rate=rate, cap=cap, quota=quota, metric=metric,
-              seed=seed)
+              seed=seed, gathered=gathered)
     torch.cuda.synchronize()
     return ab, phi
 
@@ -95,14 +95,17 @@ def check_set_agreement(keep_gpu, ref_score, off, quota):
         assert np.array_equal(keep_gpu[lo:hi][clear].astype(bool), want[clear]), f"expert {e}"
 
 
-def check_compaction(pipe, inp_np, perm, sel_off, sel_pos, ab_np, phi_np, K, dtype):
+def check_compaction(pipe, inp_np, perm, sel_off, sel_pos, ab_np, phi_np, K, dtype,
+                     copies=True):
+    """Compacted rows and maps; `copies=False` when only the gradient rows
+    were written (the products read x, ab and phi in place)."""
     M = int(sel_off[-1])
     c = oracle.compact(perm, sel_off, sel_pos, inp_np["alpha"], inp_np["x"], inp_np["g"],
                        ab_np, phi_np, K)
     assert np.array_equal(to_np(pipe.tok_c)[:M], c["tok_c"])
     N = perm.shape[0]
     assert np.array_equal(to_np(pipe.row_of_pos)[:N], c["row_of_pos"])
-    for name in ("x_c", "ab_c", "phi_c"):  # pure copies: bitwise
+    for name in ("x_c", "ab_c", "phi_c") if copies else ():  # pure copies: bitwise
         assert np.array_equal(to_np(getattr(pipe, name))[:M], c[name]), name
     dy = to_np(pipe.dy_c)[:M].astype(np.float64)
     # one rounding of alpha*g to the layer dtype

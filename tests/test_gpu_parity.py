@@ -38,7 +38,7 @@ def _to(inp, dev):
 
 
 def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None, metric=0, rseed=0,
-                inp_cpu=None):
+                inp_cpu=None, gathered=False):
     """Every step of the path against the oracle on one seeded layer; `metric`
     and `rseed` pick the selection criterion and the random criterion's seed;
     `inp_cpu` replaces the generated layer."""
@@ -47,7 +47,10 @@ def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None, metric=0, rseed=0,
     inp = _to(inp_cpu, dev)
     pipe = _pipe(cfg, dev)
     q_t = None if quota is None else torch.as_tensor(quota, dtype=torch.int32, device=dev)
-    run_gpu(pipe, inp, rate, cap, q_t, metric, rseed)
+    if gathered:  # rows the gathered products must not need
+        for k in ("x_c", "ab_c", "phi_c"):
+            getattr(pipe, k).fill_(float("nan"))
+    run_gpu(pipe, inp, rate, cap, q_t, metric, rseed, gathered)
     assert pipe.device_error() == 0
     nin = numpy_inputs(inp_cpu)
     perm, inv, counts, off = check_dispatch(pipe, nin["topk_idx"], cfg.E)
@@ -65,7 +68,8 @@ def full_parity(cfg, dev, rate, cap=0, quota=None, seed=None, metric=0, rseed=0,
         check_scores(to_np(pipe.score)[:N], ref_score)
     keep, sel_off, sel_pos = check_selection(pipe, perm, off, qv)
     check_set_agreement(keep, ref_score, off, qv)
-    c = check_compaction(pipe, nin, perm, sel_off, sel_pos, ab, phi, cfg.K, cfg.dtype)
+    c = check_compaction(pipe, nin, perm, sel_off, sel_pos, ab, phi, cfg.K, cfg.dtype,
+                         copies=not gathered)
     errs = check_backward(pipe, nin, c, sel_off, inv, cfg.T, cfg.K, cfg.dtype)
     return pipe, errs
 
@@ -427,3 +431,65 @@ def test_recompute_stress_edge_groups(dev):
 def test_recompute_zero_retention(dev):
     cfg = get_config("qwen3-30b-a3b-t4k", T=256, D=128, H=64, E=8, K=2)
     recompute_parity(cfg, dev, (0, 1))
+
+
+# ---------------------------------------------------------------------------
+# products reading x, [a | b] and phi rows in place (TMA gather4)
+# ---------------------------------------------------------------------------
+def gathered_equals_compacted(cfg, dev, rate, cap=0, inp=None):
+    """The gathered backward gives the compacted backward's results bit for
+    bit: the same tiles and reduction order, only the operand source differs."""
+    if inp is None:
+        inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    run_gpu(pipe, inp, rate, cap)
+    keys = ("dy_c", "tok_c", "row_of_pos", "dab_c", "dx_c", "dw_gate", "dw_up", "dw_down", "dx")
+    ref = {k: getattr(pipe, k).clone() for k in keys}
+    M = pipe.retained_rows
+    for k in ("x_c", "ab_c", "phi_c", "dab_c", "dx_c", "dw_gate", "dw_up", "dw_down", "dx"):
+        getattr(pipe, k).fill_(float("nan"))
+    run_gpu(pipe, inp, rate, cap, gathered=True)
+    assert pipe.device_error() == 0
+    for k, v in ref.items():
+        got = getattr(pipe, k)
+        if k in ("dy_c", "tok_c", "dab_c", "dx_c"):
+            got, v = got[:M], v[:M]
+        assert torch.equal(got, v), k
+    assert bool(torch.isnan(pipe.x_c[:max(M, 1)]).all())  # never written
+    return pipe
+
+
+@pytest.mark.parametrize("rate", [(1, 2), (3, 5), (1, 1)])
+def test_gathered_bf16_ragged_tiles_vs_oracle(dev, rate):
+    cfg = get_config("qwen3-30b-a3b-t4k", T=1024, D=320, H=192, E=12, K=3)
+    full_parity(cfg, dev, rate, gathered=True)
+
+
+def test_gathered_fp32_vs_oracle(dev):
+    full_parity(get_config("tiny", T=200, D=48, H=40, E=6, K=3), dev, (3, 5), gathered=True)
+
+
+def test_gathered_stress_vs_oracle(dev):
+    full_parity(get_config("stress-e256", T=2048, D=256, H=128), dev, (1, 2), cap=100,
+                gathered=True)
+
+
+@pytest.mark.parametrize("rate", [(1, 2), (0, 1), (1, 1)])
+def test_gathered_equals_compacted_bitwise(dev, rate):
+    gathered_equals_compacted(
+        get_config("glm45-106b-a12b-t16k", T=768, D=512, H=320, E=24, K=4), dev, rate)
+
+
+def test_gathered_equals_compacted_full_size(dev):
+    cfg = get_config("qwen3-30b-a3b-t4k")
+    gathered_equals_compacted(cfg, dev, (3, 5), inp=generate(cfg, device=dev))
+
+
+def test_gathered_equals_compacted_full_size_three_stage_ring(dev):
+    # 256 experts leave shared memory for a 3-stage operand ring only
+    cfg = get_config("stress-e256")
+    gathered_equals_compacted(cfg, dev, (1, 2), cap=cfg.cap, inp=generate(cfg, device=dev))
+
+
+def test_gathered_equals_compacted_fp32(dev):
+    gathered_equals_compacted(get_config("tiny"), dev, (1, 2))
