@@ -142,10 +142,10 @@ lrm_status lrm_score(const lrm_shape* shape, const void* g, const void* phi,
  * The selection criteria LRMoE Sec. 4.7 (Table 2) compares LRM against,
  * computed like lrm_score and written to score [N] in dispatch order:
  *   LRM_METRIC_LRM       alpha_u^2 ||g_t||^2 ||phi_u||^2   (= lrm_score)
- *   LRM_METRIC_GRAD_SQ   ||g_t||_2^2       the "squared gradient norm"
- *   LRM_METRIC_GRAD_ABS  sum_d |g_t,d|     the "absolute gradient magnitude"
+ *   LRM_METRIC_GRAD_SQ   ||g_t||_2^2       squared gradient norm
+ *   LRM_METRIC_GRAD_ABS  sum_d |g_t,d|     absolute gradient magnitude
  *   LRM_METRIC_RANDOM    output p+1 of SplitMix64 seeded with `seed`, top 24
- *                        bits as a float in [0,1): "pure random selection"
+ *                        bits as a float in [0,1): random selection
  * The gradient-only criteria read g only (alpha and phi may be NULL); the
  * random one reads neither (g may be NULL too). All are non-negative, so
  * lrm_select_quota applies to them unchanged.
@@ -287,8 +287,8 @@ lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* shape,
 /*
  * The five sub-steps of lrm_expert_bwd_grouped as separate calls, same
  * arithmetic, arguments and layouts as documented there (LRMoE Sec. 3.4:
- * "the FC1 and FC2 data-gradient and weight-gradient operations" over the
- * retained rows). Issue them in this order on one stream; each reads only
+ * both layers' data- and weight-gradient products run over the retained
+ * rows). Issue them in this order on one stream; each reads only
  * what the earlier ones wrote.
  *   lrm_expert_fc2_dgrad : dab_c = SwiGLU-grad(dy_c W_down[e]^T, ab_c)
  *   lrm_expert_fc2_wgrad : dW_down[e] = phi_c^T dy_c        (overwritten)

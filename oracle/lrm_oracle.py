@@ -216,7 +216,7 @@ def select_quota(R, off, quota, perm):
     optimal; solutions differ only among tied boundary scores.
     READING: ties are broken by the lower pair index p = t*K + k.
     READING: retained rows are listed in ascending dispatch position
-    ("consistent pair order", [LRMoE] Sec. 3.1 "compact runtime").
+    ([LRMoE] Sec. 3.1, compact runtime: retained pairs keep one consistent order).
 
     Returns (keep uint8 [N] in dispatch order, sel_off int64 [E+1] =
     exclusive scan of the quotas, sel_pos int64 [M] retained dispatch
