@@ -89,7 +89,7 @@ struct Params {
   int selftest;      // 1: the copy warp delivers nothing (bounded-wait self-test)
   int E, D, H;
   int n_rows;      // row capacity of the compacted buffers
-  int stage_bufs;  // 32x32 fp32 staging blocks per epilogue warp (0, 1 or 2)
+  int stage_bufs;  // 32x32 fp32 staging blocks per epilogue warp (0 to 3)
   int stages;      // depth of the operand ring (3 or 4)
   const int32_t* sel_off;
   const __nv_bfloat16* ab_c;
@@ -240,7 +240,9 @@ __device__ __forceinline__ void bulk_commit() {
 }
 // wait until at most `pending` committed bulk groups may still read shared memory
 __device__ __forceinline__ void bulk_wait_read(int pending) {
-  if (pending > 0)
+  if (pending >= 2)
+    asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+  else if (pending == 1)
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
   else
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -967,7 +969,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
         bulk_commit();
       }
-      if (nbuf == 2) buf ^= 1;
+      if (++buf == nbuf) buf = 0;
     };
 
     for (int tau = unit; tau < sc.total; tau += units) {
@@ -1186,11 +1188,17 @@ static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs
 #ifndef LRM_TC_STAGE_BUFS
 #define LRM_TC_STAGE_BUFS 1
 #endif
+// the same for the weight-gradient products, whose epilogue stores bound them
+#ifndef LRM_TC_WG_STAGE_BUFS
+#define LRM_TC_WG_STAGE_BUFS 1
+#endif
 
 template <int MODE, bool PAIR>
 static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStream_t cs) {
   constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
-  p.stage_bufs = (MODE == kG1 || Geo<MODE>::kFwd) ? 0 : LRM_TC_STAGE_BUFS;
+  p.stage_bufs = (MODE == kG1 || Geo<MODE>::kFwd) ? 0
+                 : Geo<MODE>::kWgrad                ? LRM_TC_WG_STAGE_BUFS
+                                                    : LRM_TC_STAGE_BUFS;
   p.stages = MAX_STAGES;
   while (p.stages > 2 && smem_bytes(p.E, p.stages, STB, p.stage_bufs) > kSmemLimit) --p.stages;
   const size_t smem = smem_bytes(p.E, p.stages, STB, p.stage_bufs);
