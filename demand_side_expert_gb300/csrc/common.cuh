@@ -66,6 +66,34 @@ inline lrm_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
 }
 
+// Programmatic dependent launch. Every kernel of the path is launched with
+// the attribute below and starts with pdl_begin(): it waits until the grid
+// before it in the stream has completed and its writes are visible, then
+// lets the next grid be scheduled. So the next kernel's CTAs can be resident
+// (and run setup that touches no global memory) while this one drains, and
+// no kernel touches global memory before its predecessor is complete. A
+// kernel launched without the attribute, or after a non-kernel operation,
+// waits for nothing extra.
+#ifndef LRM_PDL
+#define LRM_PDL 1
+#endif
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = LRM_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 inline int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -77,6 +105,15 @@ inline int num_sms() {
 // ---------------------------------------------------------------------------
 // device helpers
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_begin() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
+
 __device__ __forceinline__ void flag_error(int32_t* err, int32_t bit) {
   if (err) atomicOr(err, bit);
 }

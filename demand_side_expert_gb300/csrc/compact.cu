@@ -28,6 +28,7 @@ compact_kernel(const int32_t* __restrict__ perm, const uint8_t* __restrict__ kee
                T* __restrict__ phi_c, int32_t* __restrict__ tok_c,
                int32_t* __restrict__ row_of_pos, int ntok, int D, int H, int K, int E,
                int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   constexpr int V = Vec16<T>::kElems;
   const int64_t N = (int64_t)ntok * K;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(256)
 dx_gather_kernel(const float* __restrict__ dx_c, const int32_t* __restrict__ inv,
                  const int32_t* __restrict__ row_of_pos, float* __restrict__ dx, int ntok,
                  int D, int K, int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   const int lane = threadIdx.x & 31;
   const int64_t N = (int64_t)ntok * K;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -124,7 +126,7 @@ lrm_status launch_dx_gather(const lrm_shape* s, const float* dx_c, const int32_t
   if (s->T == 0) return LRM_OK;
   const int64_t cap = (int64_t)num_sms() * 64;
   const int blocks = (int)((std::min<int64_t>(s->T, cap) + 7) / 8);
-  dx_gather_kernel<<<blocks, 256, 0, cs>>>(dx_c, inv, row_of_pos, dx, s->T, s->D, s->K, err);
+  launch_k(dx_gather_kernel, dim3(blocks), dim3(256), 0, cs, dx_c, inv, row_of_pos, dx, s->T, s->D, s->K, err);
   return launch_status();
 }
 
@@ -156,13 +158,13 @@ extern "C" lrm_status lrm_compact(const lrm_shape* s, const int32_t* perm,
   cudaStream_t cs = (cudaStream_t)stream;
   if (s->dtype == LRM_BF16) {
     using T = __nv_bfloat16;
-    compact_kernel<T><<<blocks, 256, 0, cs>>>(
+    launch_k(compact_kernel<T>, dim3(blocks), dim3(256), 0, cs, 
         perm, keep, sel_off, sel_pos, alpha, (const T*)x, (const T*)g, (const T*)ab,
         (const T*)phi, (T*)dy_c, (T*)x_c, (T*)ab_c, (T*)phi_c, tok_c, row_of_pos, s->T, s->D,
         s->H, s->K, s->E, error_word(ws));
   } else {
     using T = float;
-    compact_kernel<T><<<blocks, 256, 0, cs>>>(
+    launch_k(compact_kernel<T>, dim3(blocks), dim3(256), 0, cs, 
         perm, keep, sel_off, sel_pos, alpha, (const T*)x, (const T*)g, (const T*)ab,
         (const T*)phi, (T*)dy_c, (T*)x_c, (T*)ab_c, (T*)phi_c, tok_c, row_of_pos, s->T, s->D,
         s->H, s->K, s->E, error_word(ws));

@@ -64,6 +64,7 @@ __device__ __forceinline__ void chunk_histogram(const int32_t* __restrict__ idx,
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_hist_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int nblk,
                      int32_t* __restrict__ chunk_hist, int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   extern __shared__ int32_t sh[];
   chunk_histogram(idx, N, E, sh, err);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(1024)
 dispatch_scan_kernel(const int32_t* __restrict__ chunk_hist, int E, int nblk,
                      int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
                      int32_t* __restrict__ off) {
+  pdl_begin();  // predecessor complete before any global access
   __shared__ int warp_tot[32];
   __shared__ int total;
   const int e = threadIdx.x;
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kDispThreads)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int nblk,
                         const int32_t* __restrict__ chunk_base,
                         int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  pdl_begin();  // predecessor complete before any global access
   extern __shared__ int32_t sh[];
   int32_t* hist = sh;                       // [8][E]
   int32_t* run = sh + kDispWarps * E;       // [8][E] next position per warp
@@ -197,6 +200,7 @@ __global__ void __cluster_dims__(kFusedCtas, 1, 1) __launch_bounds__(kFusedThrea
 dispatch_fused_kernel(const int32_t* __restrict__ idx, int64_t N, int E,
                       int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                       int32_t* __restrict__ counts, int32_t* __restrict__ off, int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   extern __shared__ int32_t sh[];
   int32_t* wh = sh;                        // [32 warps][E]: counts, then exclusive bases
   int32_t* cta_cnt = sh + kFusedWarps * E;  // [E] this CTA's counts (read by peers)
@@ -280,6 +284,7 @@ dispatch_fused_kernel(const int32_t* __restrict__ idx, int64_t N, int E,
 __global__ void permute_rows_kernel(const int32_t* __restrict__ perm, int n_rows,
                                     const uint4* __restrict__ src, uint4* __restrict__ dst,
                                     int64_t vec_per_row) {
+  pdl_begin();  // predecessor complete before any global access
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -294,6 +299,7 @@ __global__ void permute_rows_kernel(const int32_t* __restrict__ perm, int n_rows
 
 __global__ void quota_kernel(const int32_t* __restrict__ counts, int E, int num, int den,
                              int cap, int32_t* __restrict__ quota) {
+  pdl_begin();  // predecessor complete before any global access
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   const int64_t n = counts[e];
@@ -358,7 +364,7 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
         cudaFuncSetAttribute(dispatch_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)shf) != cudaSuccess)
       return LRM_ERR_CUDA;
-    dispatch_fused_kernel<<<kFusedCtas, kFusedThreads, shf, cs>>>(
+    launch_k(dispatch_fused_kernel, dim3(kFusedCtas), dim3(kFusedThreads), shf, cs, 
         topk_idx, N, E, perm, inv, counts, off, error_word(ws));
     return launch_status();
   }
@@ -373,10 +379,10 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
     cudaFuncSetAttribute(dispatch_scatter_kernel,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh3);
   }
-  dispatch_hist_kernel<<<nblk, kDispThreads, sh1, cs>>>(topk_idx, N, E, nblk, chunk_hist,
+  launch_k(dispatch_hist_kernel, dim3(nblk), dim3(kDispThreads), sh1, cs, topk_idx, N, E, nblk, chunk_hist,
                                                         error_word(ws));
-  dispatch_scan_kernel<<<1, 1024, 0, cs>>>(chunk_hist, E, nblk, chunk_base, counts, off);
-  dispatch_scatter_kernel<<<nblk, kDispThreads, sh3, cs>>>(topk_idx, N, E, nblk,
+  launch_k(dispatch_scan_kernel, dim3(1), dim3(1024), 0, cs, chunk_hist, E, nblk, chunk_base, counts, off);
+  launch_k(dispatch_scatter_kernel, dim3(nblk), dim3(kDispThreads), sh3, cs, topk_idx, N, E, nblk,
                                                            chunk_base, perm, inv);
   return launch_status();
 }
@@ -390,7 +396,7 @@ extern "C" lrm_status lrm_permute_rows(const int32_t* perm, int32_t n_rows, cons
   const int64_t vec = row_bytes / 16;
   const int64_t warps = std::min<int64_t>(n_rows, (int64_t)num_sms() * 64);
   const int blocks = (int)((warps + 7) / 8);
-  permute_rows_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(
+  launch_k(permute_rows_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, 
       perm, n_rows, (const uint4*)src, (uint4*)dst, vec);
   return launch_status();
 }
@@ -400,7 +406,7 @@ extern "C" lrm_status lrm_quota_from_rate(const int32_t* counts, int32_t E, int3
                                           void* stream) {
   if (E <= 0 || den <= 0 || num < 0 || num > den) return LRM_ERR_INVALID_ARG;
   if (!counts || !quota) return LRM_ERR_INVALID_ARG;
-  quota_kernel<<<(E + 255) / 256, 256, 0, (cudaStream_t)stream>>>(counts, E, num, den, cap,
+  launch_k(quota_kernel, dim3((E + 255) / 256), dim3(256), 0, (cudaStream_t)stream, counts, E, num, den, cap,
                                                                   quota);
   return launch_status();
 }

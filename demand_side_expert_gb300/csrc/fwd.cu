@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256)
 gather_tokens_kernel(const int32_t* __restrict__ perm, const uint4* __restrict__ x,
                      uint4* __restrict__ x_disp, int64_t N, int K, int64_t ntok, int vec_per_row,
                      int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ y, const float* __restrict__ alpha,
                const int32_t* __restrict__ inv, float* __restrict__ out, int ntok, int D, int K,
                int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   constexpr int V = Vec16<T>::kElems;
   const int lane = threadIdx.x & 31;
   const int64_t N = (int64_t)ntok * K;
@@ -93,7 +95,7 @@ static lrm_status launch_gather(const lrm_shape* s, const int32_t* perm, const v
   const int64_t N = (int64_t)s->T * s->K;
   if (N == 0) return LRM_OK;
   const int vec = s->D * elem_bytes(s->dtype) / 16;
-  gather_tokens_kernel<<<warp_grid(N), 256, 0, cs>>>(perm, (const uint4*)x, (uint4*)x_disp, N,
+  launch_k(gather_tokens_kernel, dim3(warp_grid(N)), dim3(256), 0, cs, perm, (const uint4*)x, (uint4*)x_disp, N,
                                                      s->K, s->T, vec, err);
   return launch_status();
 }
@@ -102,10 +104,10 @@ static lrm_status launch_combine(const lrm_shape* s, const void* y, const float*
                                  const int32_t* inv, float* out, int32_t* err, cudaStream_t cs) {
   if (s->T == 0) return LRM_OK;
   if (s->dtype == LRM_BF16)
-    combine_kernel<__nv_bfloat16><<<warp_grid(s->T), 256, 0, cs>>>(
+    launch_k(combine_kernel<__nv_bfloat16>, dim3(warp_grid(s->T)), dim3(256), 0, cs, 
         (const __nv_bfloat16*)y, alpha, inv, out, s->T, s->D, s->K, err);
   else
-    combine_kernel<float><<<warp_grid(s->T), 256, 0, cs>>>((const float*)y, alpha, inv, out,
+    launch_k(combine_kernel<float>, dim3(warp_grid(s->T)), dim3(256), 0, cs, (const float*)y, alpha, inv, out,
                                                            s->T, s->D, s->K, err);
   return launch_status();
 }

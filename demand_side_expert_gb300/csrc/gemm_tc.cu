@@ -567,12 +567,42 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
-  // --- set-up: validated group offsets, tile table, barriers, TMEM -------
+  // --- set-up that reads nothing a kernel writes: barriers, TMEM, maps ----
   if (tid == 0) {
     *abort_flag = 0;
     *bad_flag = 0;
+    // full: the copy warp's arrival (two in a pair's even CTA), plus one per
+    // lane of the copy warp when it gathers A rows with async copies
+    const uint32_t full_count = (PAIR && leader) ? 2u : (NG > 0 && p.a_rows) ? 33u : 1u;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], full_count);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiWarps * (PAIR ? 2 : 1));
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (warp == 0 && lane == 0 && !p.selftest) {
+    prefetch_map(mapA);
+    prefetch_map(mapB);
+    if (MODE == kG4 || MODE == kF1) prefetch_map(mapB2);
+  }
+  if (warp == 1) {
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
+  }
+  // --- the previous kernel in the stream is complete from here on ----------
+  pdl_begin();
   __syncthreads();
+  // --- validated group offsets and the tile table --------------------------
   for (int i = tid; i <= E; i += NT) {
     const int v = p.sel_off[i];
     const int prev = i > 0 ? p.sel_off[i - 1] : 0;
@@ -640,35 +670,6 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       if (lane == 0) tab[E] = carry;
     }
     sc.tpre = tab;
-  }
-  if (tid == 0) {
-    // full: the copy warp's arrival (two in a pair's even CTA), plus one per
-    // lane of the copy warp when it gathers A rows with async copies
-    const uint32_t full_count = (PAIR && leader) ? 2u : (NG > 0 && p.a_rows) ? 33u : 1u;
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], full_count);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps * (PAIR ? 2 : 1));
-    }
-    mbar_init(drain, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0 && lane == 0 && !p.selftest) {
-    prefetch_map(mapA);
-    prefetch_map(mapB);
-    if (MODE == kG4 || MODE == kF1) prefetch_map(mapB2);
-  }
-  if (warp == 1) {
-    if constexpr (PAIR) {
-      tmem_alloc_pair(tmem_slot, TMEM_COLS);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(tmem_slot, TMEM_COLS);
-      tmem_relinquish();
-    }
   }
   tc_fence_before();
   if constexpr (PAIR) cluster_sync(); else __syncthreads();
@@ -1215,15 +1216,22 @@ static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStr
   cfg.blockDim = dim3(Threads<MODE, PAIR>::kCount, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = cs;
-  cudaLaunchAttribute attr[1];
-  if (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (LRM_PDL) {  // see launch_k: the kernel starts with pdl_begin()
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
+  if (PAIR) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   if (cudaLaunchKernelEx(&cfg, kern, maps, p) != cudaSuccess) return LRM_ERR_CUDA;
   return launch_status();
 }

@@ -78,6 +78,7 @@ score_kernel(const T* __restrict__ g, const T* __restrict__ phi,
              const float* __restrict__ alpha, const int32_t* __restrict__ inv,
              float* __restrict__ score, int ntok, int D, int H, int K, uint64_t seed,
              int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   constexpr int V = Vec16<T>::kElems;
   const int lane = threadIdx.x & 31;
   const int64_t N = (int64_t)ntok * K;
@@ -139,19 +140,19 @@ static void launch_score(const lrm_shape* s, int metric, uint64_t seed, const vo
   const T* pt = (const T*)phi;
   switch (metric) {
     case LRM_METRIC_GRAD_SQ:
-      score_kernel<T, LRM_METRIC_GRAD_SQ><<<blocks, kScoreThreads, 0, cs>>>(
+      launch_k(score_kernel<T, LRM_METRIC_GRAD_SQ>, dim3(blocks), dim3(kScoreThreads), 0, cs, 
           gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
       break;
     case LRM_METRIC_GRAD_ABS:
-      score_kernel<T, LRM_METRIC_GRAD_ABS><<<blocks, kScoreThreads, 0, cs>>>(
+      launch_k(score_kernel<T, LRM_METRIC_GRAD_ABS>, dim3(blocks), dim3(kScoreThreads), 0, cs, 
           gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
       break;
     case LRM_METRIC_RANDOM:
-      score_kernel<T, LRM_METRIC_RANDOM><<<blocks, kScoreThreads, 0, cs>>>(
+      launch_k(score_kernel<T, LRM_METRIC_RANDOM>, dim3(blocks), dim3(kScoreThreads), 0, cs, 
           gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
       break;
     default:
-      score_kernel<T, LRM_METRIC_LRM><<<blocks, kScoreThreads, 0, cs>>>(
+      launch_k(score_kernel<T, LRM_METRIC_LRM>, dim3(blocks), dim3(kScoreThreads), 0, cs, 
           gt, pt, alpha, inv, score, s->T, s->D, s->H, s->K, seed, err);
   }
 }

@@ -60,6 +60,7 @@ select_kernel(const float* __restrict__ score, const int32_t* __restrict__ off,
               const int32_t* __restrict__ quota, int E, int keys_cap,
               uint8_t* __restrict__ keep, int32_t* __restrict__ sel_off,
               int32_t* __restrict__ sel_pos, int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
   extern __shared__ uint32_t keys[];
   __shared__ uint32_t hist[256];
   __shared__ int scratch[kSelWarps];
@@ -222,7 +223,7 @@ extern "C" lrm_status lrm_select_quota(const lrm_shape* s, const float* score,
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
-  select_kernel<<<s->E, kSelThreads, smem, (cudaStream_t)stream>>>(
+  launch_k(select_kernel, dim3(s->E), dim3(kSelThreads), smem, (cudaStream_t)stream, 
       score, off, quota, s->E, keys_cap, keep, sel_off, sel_pos, error_word(ws));
   return launch_status();
 }
