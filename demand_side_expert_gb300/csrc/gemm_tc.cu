@@ -680,18 +680,24 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   // stage s's rows [valid, 16 * ceil(valid / 16)) of every box of this CTA
   // belong to the next group or lie past the retained rows: zero them
   auto zero_tail = [&](uint8_t* a_s, int valid) {
-    const int zrows = 16 * ((valid + 15) >> 4) - valid;
-    uint8_t* b_s = a_s + A_BYTES;
-    for (int idx = lane; idx < zrows * NBOX * 8; idx += 32) {
-      const int c16 = idx & 7;
-      const int rz = (idx >> 3) % zrows;
-      const int bx = (idx >> 3) / zrows;
-      uint8_t* box = bx < BM / 64 ? a_s + bx * BOX_BYTES : b_s + (bx - BM / 64) * BOX_BYTES;
-      *reinterpret_cast<uint4*>(box + (valid + rz) * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+    const int n = (16 * ((valid + 15) >> 4) - valid) * 8;  // 16-byte chunks per box
+#pragma unroll
+    for (int bx = 0; bx < NBOX; ++bx) {
+      uint8_t* row0 = (bx < BM / 64 ? a_s + bx * BOX_BYTES
+                                    : a_s + A_BYTES + (bx - BM / 64) * BOX_BYTES) +
+                      valid * 128;
+      for (int idx = lane; idx < n; idx += 32)  // whole 128-byte rows: no swizzle
+        *reinterpret_cast<uint4*>(row0 + (idx >> 3) * 128 + (idx & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
     }
     fence_async_smem();
     __syncwarp();
   };
+
+  // Tile r of this unit (CTA or CTA pair): serpentine over the units, so that
+  // with tiles sorted longest first (weight-gradient products) every unit's
+  // total stays close to the mean. Every role walks the same sequence.
+  auto tile_of = [&](int r) { return r * units + ((r & 1) ? units - 1 - unit : unit); };
 
   if (warp == 0) {
     // ===================== TMA producer =====================
@@ -700,7 +706,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       uint32_t issued_mask = 0, issued_parity = 0;
       uint32_t tail_parity = 0;  // odd CTA of a pair: its own full barriers flip only on tails
       bool stop = false;
-      for (int tau = unit; tau < sc.total && !stop; tau += units) {
+      for (int ri = 0, tau = tile_of(0); tau < sc.total && !stop; tau = tile_of(++ri)) {
         const Tile t = decode<MODE>(sc, tau, rank);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_ns)) {
@@ -788,7 +794,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     constexpr uint32_t idesc = idesc_bf16(Cfg<PAIR>::kTileRows, BN, AMN ? 1 : 0, BMN ? 1 : 0);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool stop = false, issued_any = false;
-    for (int tau = unit; tau < sc.total && !stop; tau += units) {
+    for (int ri = 0, tau = tile_of(0); tau < sc.total && !stop; tau = tile_of(++ri)) {
       const Tile t = decode<MODE>(sc, tau, rank);
       if (t.nkb <= 0) continue;
       if (!warp_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, p.wait_ns)) break;
@@ -856,7 +862,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     if constexpr (PAIR && WG) {
       uint32_t stage = 0, tparity = 0;
       bool stop = false;
-      for (int tau = unit; tau < sc.total && !stop; tau += units) {
+      for (int ri = 0, tau = tile_of(0); tau < sc.total && !stop; tau = tile_of(++ri)) {
         const Tile t = decode<MODE>(sc, tau, rank);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (kb == t.nkb - 1 && (t.valid & 15)) {
@@ -899,7 +905,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const char* src_base = reinterpret_cast<const char*>(p.a_src);
         uint32_t it = 0;  // K blocks of this CTA so far
         bool stop = false;
-        for (int tau = unit; tau < sc.total && !stop; tau += units) {
+        for (int ri = 0, tau = tile_of(0); tau < sc.total && !stop; tau = tile_of(++ri)) {
           const Tile t = decode<MODE>(sc, tau, rank);
           const int gend = t.row0 + (t.nkb - 1) * BK + t.valid;  // group end
           for (int kb = 0; kb < t.nkb; ++kb, ++it) {
@@ -973,7 +979,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       if (++buf == nbuf) buf = 0;
     };
 
-    for (int tau = unit; tau < sc.total; tau += units) {
+    for (int ri = 0, tau = tile_of(0); tau < sc.total; tau = tile_of(++ri)) {
       const Tile t = decode<MODE>(sc, tau, rank);
       if (t.nkb <= 0) {
         // expert without retained rows: its weight gradient is zero
