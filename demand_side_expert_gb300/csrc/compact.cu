@@ -39,6 +39,12 @@ compact_kernel(const int32_t* __restrict__ perm, const uint8_t* __restrict__ kee
   const int lane = threadIdx.x & 31;
   const int64_t M = sel_off[E];
   const int dv = D / V, abv = 2 * H / V, hv = H / V;
+  {  // 64 zero rows of dy_c after the retained ones: the padding the FC2
+     // weight-gradient product reads as B past the last group
+    const int64_t zrows = M < N ? min((int64_t)64, N - M) : 0;
+    uint4* z = reinterpret_cast<uint4*>(dy_c + M * D);
+    for (int64_t i = gtid; i < zrows * dv; i += nthr) z[i] = make_uint4(0, 0, 0, 0);
+  }
   for (int64_t j = gtid >> 5; j < M; j += nthr >> 5) {
     const int i = sel_pos[j];
     const int p = (i >= 0 && i < N) ? perm[i] : -1;

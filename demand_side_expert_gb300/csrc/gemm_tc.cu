@@ -615,6 +615,17 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     if (tid == 0) flag_error(p.err, LRM_DEVERR_INDEX);
   }
   __syncthreads();
+  if constexpr (MODE == kG1) {
+    // 64 zero rows after the retained ones: the padding the FC1 weight-gradient
+    // product reads as B past the last group (see zero_tail)
+    if (blockIdx.x == 0 && p.dab_c) {
+      const int64_t m = goff[E];
+      const int64_t rows = min((int64_t)BK, (int64_t)p.n_rows - m);
+      const int64_t n16 = rows * 2 * p.H / 8;  // 16-byte chunks
+      uint4* z = reinterpret_cast<uint4*>(p.dab_c + m * 2 * p.H);
+      for (int64_t i = tid; i < n16; i += NT) z[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
 
   Sched sc;
   sc.goff = goff;
@@ -679,13 +690,18 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
 
   // stage s's rows [valid, 16 * ceil(valid / 16)) of every box of this CTA
   // belong to the next group or lie past the retained rows: zero them
+  // Rows past the group end in the last K block: a product term vanishes if
+  // its A row is zero and its B row finite. B rows there are the next group's
+  // (finite), or rows past the retained rows, which the kernels producing
+  // the B operands write as zeros for 64 rows (dy_c: the compaction; dab_c:
+  // the FC2 dgrad product), or rows past the buffer (zero-filled by TMA). So
+  // only the A boxes' rows [valid, 16 * ceil(valid / 16)) are zeroed here
+  // (gathered A rows arrive zero-filled and need nothing).
   auto zero_tail = [&](uint8_t* a_s, int valid) {
     const int n = (16 * ((valid + 15) >> 4) - valid) * 8;  // 16-byte chunks per box
 #pragma unroll
-    for (int bx = 0; bx < NBOX; ++bx) {
-      uint8_t* row0 = (bx < BM / 64 ? a_s + bx * BOX_BYTES
-                                    : a_s + A_BYTES + (bx - BM / 64) * BOX_BYTES) +
-                      valid * 128;
+    for (int bx = 0; bx < BM / 64; ++bx) {
+      uint8_t* row0 = a_s + bx * BOX_BYTES + valid * 128;
       for (int idx = lane; idx < n; idx += 32)  // whole 128-byte rows: no swizzle
         *reinterpret_cast<uint4*>(row0 + (idx >> 3) * 128 + (idx & 7) * 16) =
             make_uint4(0, 0, 0, 0);
@@ -812,7 +828,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         if constexpr (WG) {
           // rows written by async copies (generic proxy) before the MMA reads them
           if (NG > 0 && p.a_rows) fence_async_smem();
-          if (valid & 15) zero_tail(a_s, valid);
+          if ((valid & 15) && !(NG > 0 && p.a_rows)) zero_tail(a_s, valid);
         }
         tc_fence_after();
         if (lane == 0) {
@@ -894,8 +910,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     // placed at its 128-byte swizzle position), and each lane arrives on the
     // stage's full barrier once its copies have landed (32 of its 33
     // arrivals; the copy warp arms it for the B tile). Rows past the group
-    // end repeat its last row (the MMA warp zeroes or skips them); rows or
-    // columns outside the source are zero-filled.
+    // end, and rows or columns outside the source, are zero-filled.
     if constexpr (NG > 0) {
       const int ng = min(NG, STAGES);
       const int g = warp - (2 + kEpiWarps);
@@ -924,7 +939,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             for (int i = 0; i < BK / 4; ++i) {
               const int r = 4 * i + (lane >> 3);  // row of the K block
               const int src = __shfl_sync(0xffffffffu, i < BK / 8 ? ia : ib, r & 31);
-              const bool row_ok = src >= 0 && src < p.a_src_rows;
+              const bool row_ok = y + r < gend && src >= 0 && src < p.a_src_rows;
 #pragma unroll
               for (int box = 0; box < BM / 64; ++box) {
                 const int col = t.cm0 + 64 * box + 8 * chunk;

@@ -194,6 +194,8 @@ lrm_status lrm_select_quota(const lrm_shape* shape, const float* score,
  *   phi [N,H] (dispatch order).
  * Outputs (capacity N rows each, first M written): dy_c [N,D], x_c [N,D],
  *   ab_c [N,2H], phi_c [N,H], tok_c [N] int32; row_of_pos [N] int32.
+ * Rows [M, min(M + 64, N)) of dy_c are written as zeros: the weight-gradient
+ * products read them as padding past the last group.
  * x_c, ab_c and phi_c may each be NULL: that copy is skipped and its source
  * may be NULL too (see lrm_expert_fc1_recompute, which rebuilds [a | b], and
  * lrm_expert_bwd_gathered, which reads x, ab and phi rows in place). A
@@ -290,7 +292,9 @@ lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* shape,
  * both layers' data- and weight-gradient products run over the retained
  * rows). Issue them in this order on one stream; each reads only
  * what the earlier ones wrote.
- *   lrm_expert_fc2_dgrad : dab_c = SwiGLU-grad(dy_c W_down[e]^T, ab_c)
+ *   lrm_expert_fc2_dgrad : dab_c = SwiGLU-grad(dy_c W_down[e]^T, ab_c); also
+ *                          zeroes rows [M, min(M + 64, N)) of dab_c (padding
+ *                          read by lrm_expert_fc1_wgrad past the last group)
  *   lrm_expert_fc2_wgrad : dW_down[e] = phi_c^T dy_c        (overwritten)
  *   lrm_expert_fc1_wgrad : dW_gate[e], dW_up[e] = x_c^T dab_c (overwritten)
  *   lrm_expert_fc1_dgrad : dx_c = dab_c [W_gate | W_up][e]^T
