@@ -86,30 +86,34 @@ compact_kernel(const int32_t* __restrict__ perm, const uint8_t* __restrict__ kee
 }
 
 // dx[t] = sum over the token's kept slots k (ascending) of dx_c[row].
-__global__ void __launch_bounds__(256)
+// One CTA per token, its warps splitting the D columns: each lane keeps the
+// K loads of a column group in flight, and every output element is summed in
+// slot order (the same order for every split, so the result is exact and
+// deterministic).
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(32 * kGatherWarps)
 dx_gather_kernel(const float* __restrict__ dx_c, const int32_t* __restrict__ inv,
                  const int32_t* __restrict__ row_of_pos, float* __restrict__ dx, int ntok,
                  int D, int K, int32_t* err) {
   pdl_begin();  // predecessor complete before any global access
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t N = (int64_t)ntok * K;
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t t = warp; t < ntok; t += nwarps) {
+  for (int64_t t = blockIdx.x; t < ntok; t += gridDim.x) {
     int row = -1;
     if (lane < K) {
       const int pos = inv[t * K + lane];
       if (pos >= 0 && pos < N) {
         row = row_of_pos[pos];
         if (row >= N) {
-          flag_error(err, LRM_DEVERR_INDEX);
+          if (w == 0) flag_error(err, LRM_DEVERR_INDEX);
           row = -1;
         }
-      } else {
+      } else if (w == 0) {
         flag_error(err, LRM_DEVERR_INDEX);
       }
     }
-    for (int c = lane * 4; c < D; c += 128) {
+    for (int c = (w * 32 + lane) * 4; c < D; c += 32 * kGatherWarps * 4) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int k = 0; k < K; ++k) {
         const int r = __shfl_sync(0xffffffffu, row, k);
@@ -130,9 +134,9 @@ lrm_status launch_dx_gather(const lrm_shape* s, const float* dx_c, const int32_t
                             const int32_t* row_of_pos, float* dx, int32_t* err,
                             cudaStream_t cs) {
   if (s->T == 0) return LRM_OK;
-  const int64_t cap = (int64_t)num_sms() * 64;
-  const int blocks = (int)((std::min<int64_t>(s->T, cap) + 7) / 8);
-  launch_k(dx_gather_kernel, dim3(blocks), dim3(256), 0, cs, dx_c, inv, row_of_pos, dx, s->T, s->D, s->K, err);
+  const int blocks = (int)std::min<int64_t>(s->T, (int64_t)num_sms() * 64);
+  launch_k(dx_gather_kernel, dim3(blocks), dim3(32 * kGatherWarps), 0, cs, dx_c, inv, row_of_pos,
+           dx, s->T, s->D, s->K, err);
   return launch_status();
 }
 
