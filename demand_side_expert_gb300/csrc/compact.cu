@@ -58,14 +58,25 @@ compact_kernel(const int32_t* __restrict__ perm, const uint8_t* __restrict__ kee
     const uint4* xs = reinterpret_cast<const uint4*>(x + t * D);
     uint4* dyd = reinterpret_cast<uint4*>(dy_c + j * D);
     uint4* xd = reinterpret_cast<uint4*>(x_c + j * D);
-    for (int c = lane; c < dv; c += 32) {
-      float f[V];
-      Vec16<T>::unpack(gs[c], f);
+    // up to 8 of the lane's 16-byte chunks loaded before any is written
+    for (int c0 = lane; c0 < dv; c0 += 32 * 8) {
+      uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < V; ++u) f[u] *= a;
-      dyd[c] = Vec16<T>::pack(f);
-      if (x_c) xd[c] = xs[c];
+      for (int u = 0; u < 8; ++u)
+        if (c0 + 32 * u < dv) v[u] = gs[c0 + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + 32 * u < dv) {
+          float f[V];
+          Vec16<T>::unpack(v[u], f);
+#pragma unroll
+          for (int e = 0; e < V; ++e) f[e] *= a;
+          dyd[c0 + 32 * u] = Vec16<T>::pack(f);
+        }
+      }
     }
+    if (x_c)
+      for (int c = lane; c < dv; c += 32) xd[c] = xs[c];
     // the saved-state copies are skipped when their destination is absent:
     // [a | b] recomputed, or rows gathered by the products themselves
     if (ab_c) {
