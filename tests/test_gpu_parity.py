@@ -493,3 +493,58 @@ def test_gathered_equals_compacted_full_size_three_stage_ring(dev):
 
 def test_gathered_equals_compacted_fp32(dev):
     gathered_equals_compacted(get_config("tiny"), dev, (1, 2))
+
+
+# ---------------------------------------------------------------------------
+# launches that overlap their predecessor (programmatic dependent launch)
+# ---------------------------------------------------------------------------
+def test_back_to_back_steps_without_sync_match_synchronized_steps(dev):
+    """Two layers' steps issued back to back on one stream (every kernel may be
+    scheduled while the previous one drains) give the results of steps run
+    one at a time; then the second layer's outputs are checked."""
+    cfg = get_config("qwen3-30b-a3b-t4k", T=1024, D=320, H=192, E=12, K=3)
+    a = _to(generate(cfg, device="cpu", seed=5), dev)
+    b = _to(generate(cfg, device="cpu", seed=6), dev)
+    keys = ("perm", "score", "keep", "sel_pos", "dy_c", "dab_c", "dx_c", "dw_gate", "dw_up",
+            "dw_down", "dx")
+
+    def run(pipe, inp, gathered):
+        pipe.dispatch(inp["topk_idx"])
+        abd = pipe.to_dispatch_order(inp["ab_pair"])
+        phid = pipe.to_dispatch_order(inp["phi_pair"])
+        pipe.step(inp["topk_idx"], inp["alpha"], inp["x"], inp["g"], abd, phid, inp["w_gate"],
+                  inp["w_up"], inp["w_down"], rate=(1, 2), gathered=gathered)
+
+    for gathered in (False, True):
+        ref = _pipe(cfg, dev)
+        run(ref, b, gathered)
+        torch.cuda.synchronize()
+        want = {k: getattr(ref, k).clone() for k in keys}
+        pipe = _pipe(cfg, dev)
+        for _ in range(3):  # a, b, a, b, a, b with no synchronization in between
+            run(pipe, a, gathered)
+            run(pipe, b, gathered)
+        torch.cuda.synchronize()
+        assert pipe.device_error() == 0
+        M = pipe.retained_rows
+        for k, v in want.items():
+            got = getattr(pipe, k)
+            if k in ("dy_c", "dab_c", "dx_c", "sel_pos"):
+                got, v = got[:M], v[:M]
+            assert torch.equal(got, v), (gathered, k)
+
+
+def test_padding_rows_after_the_retained_rows_are_zero(dev):
+    """The weight-gradient products read 64 rows past the last group as
+    padding; the compaction (dy_c) and the FC2 dgrad product (dab_c) write
+    them as zeros."""
+    cfg = get_config("qwen3-30b-a3b-t4k", T=512, D=256, H=128, E=8, K=2)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    pipe.dy_c.fill_(float("nan"))
+    pipe.dab_c.fill_(float("nan"))
+    run_gpu(pipe, inp, (1, 2))
+    M, N = pipe.retained_rows, cfg.N
+    hi = min(M + 64, N)
+    assert hi > M
+    assert bool((pipe.dy_c[M:hi] == 0).all()) and bool((pipe.dab_c[M:hi] == 0).all())
