@@ -1025,13 +1025,15 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
         const __nv_bfloat16* arow = p.ab_c + src * 2 * p.H;
         __nv_bfloat16* drow = p.dab_c + j * 2 * p.H;
+        const bool g1_whole = q * 32 + 32 <= t.cvalid;  // warp-uniform
         uint4 a_cur[4], b_cur[4], a_nxt[4], b_nxt[4];
         auto load_ab = [&](int h, uint4 (&av)[4], uint4 (&bv)[4]) {
           if (rv && h < p.H) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              av[v] = ld_stream(arow + h + 8 * v);
-              bv[v] = ld_stream(arow + p.H + h + 8 * v);
+              // read-only path: a row's four 16-byte pieces share its L1 lines
+              av[v] = __ldg(reinterpret_cast<const uint4*>(arow + h + 8 * v));
+              bv[v] = __ldg(reinterpret_cast<const uint4*>(arow + p.H + h + 8 * v));
             }
           }
         };
@@ -1043,7 +1045,32 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (c + 32 < c_hi) load_ab(t.n0 + c + 32, a_nxt, b_nxt);
           tmem_ld_wait();
           const int h = t.n0 + c;
-          if (rv && h < p.H) {
+          if (g1_whole && h < p.H) {
+            // the warp's 32 rows lie inside the group: stage the da and db
+            // blocks (32 rows x 64 B each, 64-byte swizzle) and write them
+            // with two TMA bulk-tensor stores
+            uint4 dav[4], dbv[4];
+            swiglu_chunk(r, a_cur, b_cur, dav, dbv);
+            if (!rv) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) dav[v] = dbv[v] = make_uint4(0, 0, 0, 0);
+            }
+            if (lane == 0) bulk_wait_read(0);
+            __syncwarp();
+            const int sw = (lane >> 1) & 3;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              *reinterpret_cast<uint4*>(wst + lane * 64 + ((v ^ sw) << 4)) = dav[v];
+              *reinterpret_cast<uint4*>(wst + 2048 + lane * 64 + ((v ^ sw) << 4)) = dbv[v];
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&maps.o1, wst, h, t.cm0 + q * 32);
+              tma_store_2d(&maps.o1, wst + 2048, p.H + h, t.cm0 + q * 32);
+              bulk_commit();
+            }
+          } else if (rv && h < p.H) {  // block crossing the group end: row by row
             uint4 dav[4], dbv[4];
             swiglu_chunk(r, a_cur, b_cur, dav, dbv);
             uint4* da_dst = reinterpret_cast<uint4*>(drow + h);
@@ -1184,7 +1211,8 @@ static EncodeTiledFn encode_fn() {
 // Row-major [rows, cols] (rank 2) or [E, rows, cols] (rank 3) map with a
 // 128-byte swizzle; bf16 operands or fp32 outputs.
 static bool make_map(CUtensorMap* m, const void* base, bool fp32, int rank, uint64_t E,
-                     uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+                     uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+                     int swizzle_bytes = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const uint64_t es = fp32 ? 4 : 2;
@@ -1194,7 +1222,8 @@ static bool make_map(CUtensorMap* m, const void* base, bool fp32, int rank, uint
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1218,7 +1247,7 @@ static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs
 template <int MODE, bool PAIR>
 static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStream_t cs) {
   constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
-  p.stage_bufs = (MODE == kG1 || Geo<MODE>::kFwd) ? 0
+  p.stage_bufs = Geo<MODE>::kFwd ? 0
                  : Geo<MODE>::kWgrad                ? LRM_TC_WG_STAGE_BUFS
                                                     : LRM_TC_STAGE_BUFS;
   p.stages = MAX_STAGES;
@@ -1337,9 +1366,13 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
         !make_map(&m1.b, a.w_down, false, 3, E, H, D, 64, BN) ||
         !make_map(&m2.b, a.w_down, false, 3, E, H, D, 64, BN / 2))
       return LRM_ERR_CUDA;
+    // dab_c as 32 x 32 bf16 blocks (64-byte rows, 64-byte swizzle) for the
+    // epilogue's staged stores
+    if (!make_map(&m1.o1, a.dab_c, false, 2, 1, rows, 2 * H, 32, 32, 64)) return LRM_ERR_CUDA;
     m2.a = m1.a;
-    m1.b2 = m1.o1 = m1.o2 = m1.b;
-    m2.b2 = m2.o1 = m2.o2 = m2.b;
+    m1.b2 = m1.o2 = m1.b;
+    m2.b2 = m2.o2 = m2.b;
+    m2.o1 = m1.o1;
     p.ab_rows = gathered ? a.sel_pos : nullptr;
     if ((st = launch_any<kG1>(m1, m2, p, dg_tiles(BM, H), dg_tiles(2 * BM, H), a.stream)) !=
         LRM_OK)
