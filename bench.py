@@ -2,10 +2,10 @@
 """Benchmark of the recalibrated MoE expert backward on GB300.
 
 One step = one pass of the whole path over one synthetic MoE layer with its
-inputs resident in HBM: dispatch permutation, quota rule, LRM score,
+inputs resident in HBM: dispatch permutation, LRM score, quota rule and
 per-expert top-q selection, compaction, the four grouped expert-backward
-products and the dx scatter (10 kernel launches up to 2^20 routed pairs). The metric is retained
-rows per second, M / step time, with M = sum_e q_e the retained
+products and the dx scatter (9 kernel launches up to 2^20 routed pairs). The metric is
+retained rows per second, M / step time, with M = sum_e q_e the retained
 token-expert pairs. The L2 is flushed (a 256 MiB write) before every timed
 step, outside the step's CUDA events.
 
@@ -35,11 +35,11 @@ if ROOT not in sys.path:
 METRIC = "retained-pair expert-backward rows/s; grouped-GEMM % BF16 peak; select GB/s"
 DEFAULT_CONFIG = "qwen3-30b-a3b-t4k"
 FLUSH_BYTES = 256 << 20
-SEGMENTS = ["dispatch", "quota", "score", "select", "compact", "fc2_dgrad", "fc2_wgrad",
+SEGMENTS = ["dispatch", "score", "select", "compact", "fc2_dgrad", "fc2_wgrad",
             "fc1_wgrad", "fc1_dgrad", "scatter_dx"]
 # kernels whose names the launch list shows for each segment
 KERNEL_NAMES = {
-    "dispatch": "dispatch_fused_kernel", "quota": "quota_kernel",
+    "dispatch": "dispatch_fused_kernel",
     "score": "score_kernel", "select": "select_kernel", "compact": "compact_kernel",
     "fc2_dgrad": "grouped_gemm_kernel<0, 1>", "fc2_wgrad": "grouped_gemm_kernel<1, 0>",
     "fc1_wgrad": "grouped_gemm_kernel<2, 0>", "fc1_dgrad": "grouped_gemm_kernel<3, 1>",
@@ -56,12 +56,12 @@ FWD_KERNEL_NAMES = {
 
 
 def kernels_per_step(N: int) -> int:
-    """Launches of one step: dispatch (1 or 3), quota, score, select, compact,
-    four grouped GEMMs, dx scatter."""
-    return (1 if N <= FUSED_DISPATCH_MAX_PAIRS else 3) + 9
+    """Launches of one step: dispatch (1 or 3), score, select (with the quota
+    rule), compact, four grouped GEMMs, dx scatter."""
+    return (1 if N <= FUSED_DISPATCH_MAX_PAIRS else 3) + 8
 # source file of each segment's kernel (for the traffic record's freshness check)
 KERNEL_SOURCE = {
-    "dispatch": "dispatch.cu", "quota": "dispatch.cu", "score": "score.cu",
+    "dispatch": "dispatch.cu", "score": "score.cu",
     "select": "select.cu", "compact": "compact.cu", "fc2_dgrad": "gemm_tc.cu",
     "fc2_wgrad": "gemm_tc.cu", "fc1_wgrad": "gemm_tc.cu", "fc1_dgrad": "gemm_tc.cu",
     "scatter_dx": "compact.cu",
@@ -107,9 +107,8 @@ def algorithmic(cfg, M: int, gathered: bool = False) -> dict:
     W = E * D * H * s  # one expert weight tensor, all experts
     return {
         "dispatch": {"bytes": 4 * N + 8 * N + 8 * E},
-        "quota": {"bytes": 8 * E},
         "score": {"bytes": T * D * s + N * H * s + 4 * N + 4 * N + 4 * N},
-        "select": {"bytes": 4 * N + N + 4 * M + 16 * E},
+        "select": {"bytes": 4 * N + N + 4 * M + 24 * E},
         "compact": {"bytes": (2 * M * D * s if gathered else 2 * M * (2 * D + 3 * H) * s)
                     + 4 * M * 4 + 5 * N},
         "fc2_dgrad": {"bytes": M * D * s + W + 2 * (M * 2 * H * s), "flops": 2 * M * D * H},
@@ -304,32 +303,30 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         mark(0)
         pipe.dispatch(inp["topk_idx"])
         mark(1)
-        pipe.quota_from_rate(rate[0], rate[1], cfg.cap)
-        mark(2)
         pipe.score_pairs(inp["alpha"], inp["g"], phi)
+        mark(2)
+        pipe.select_rate(rate[0], rate[1], cfg.cap)
         mark(3)
-        pipe.select()
-        mark(4)
         pipe.compact(inp["alpha"], inp["x"], inp["g"], ab, phi, gathered=gathered)
-        mark(5)
+        mark(4)
         if gathered:  # the products read x, ab and phi rows in place
             for j, part in enumerate((lrm.LRM_BWD_FC2_DGRAD, lrm.LRM_BWD_FC2_WGRAD,
                                       lrm.LRM_BWD_FC1_WGRAD, lrm.LRM_BWD_FC1_DGRAD,
                                       lrm.LRM_BWD_SCATTER_DX)):
                 pipe.expert_bwd_gathered(inp["x"], ab, phi, inp["w_gate"], inp["w_up"],
                                          inp["w_down"], parts=part)
-                mark(6 + j)
+                mark(5 + j)
             return
         pipe.fc2_dgrad(inp["w_down"])
-        mark(6)
+        mark(5)
         pipe.fc2_wgrad()
-        mark(7)
+        mark(6)
         pipe.fc1_wgrad()
-        mark(8)
+        mark(7)
         pipe.fc1_dgrad(inp["w_gate"], inp["w_up"])
-        mark(9)
+        mark(8)
         pipe.scatter_dx()
-        mark(10)
+        mark(9)
 
     def new_events():
         return [torch.cuda.Event(enable_timing=True) for _ in range(len(SEGMENTS) + 1)]
@@ -505,9 +502,8 @@ def run_recompute(pipe, inp, phi, rate, cfg, flush, stream, args):
     def step(ev):
         ev[0].record(stream)
         pipe.dispatch(inp["topk_idx"])
-        pipe.quota_from_rate(rate[0], rate[1], cfg.cap)
         pipe.score_pairs(inp["alpha"], inp["g"], phi)
-        pipe.select()
+        pipe.select_rate(rate[0], rate[1], cfg.cap)
         pipe.compact(inp["alpha"], inp["x"], inp["g"], None, phi)
         ev[1].record(stream)
         pipe.fc1_recompute(inp["w_gate"], inp["w_up"])

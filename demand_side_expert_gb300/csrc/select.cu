@@ -55,9 +55,25 @@ __device__ __forceinline__ int block_sum(int v, int* sh) {
   return r;
 }
 
+// Quota of an expert with n routed pairs under RATE: min(ceil(num/den * n),
+// cap), in exact integers (cap <= 0: none); otherwise the given quota.
+template <bool RATE>
+__device__ __forceinline__ int quota_of(const int32_t* quota, int j, int n, int num, int den,
+                                        int cap) {
+  if constexpr (RATE) {
+    int q = (int)(((int64_t)num * n + den - 1) / den);
+    return cap > 0 ? min(q, cap) : q;
+  } else {
+    return quota[j];
+  }
+}
+
+// RATE: the quotas are computed from the rate num/den and the cap (and
+// written to quota[e]) instead of read from quota.
+template <bool RATE>
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ score, const int32_t* __restrict__ off,
-              const int32_t* __restrict__ quota, int E, int keys_cap,
+              int32_t* __restrict__ quota, int num, int den, int cap, int E, int keys_cap,
               uint8_t* __restrict__ keep, int32_t* __restrict__ sel_off,
               int32_t* __restrict__ sel_pos, int32_t* err) {
   pdl_begin();  // predecessor complete before any global access
@@ -73,7 +89,7 @@ select_kernel(const float* __restrict__ score, const int32_t* __restrict__ off,
   int part = 0;
   for (int j = tid; j < e; j += kSelThreads) {
     const int nj = max(off[j + 1] - off[j], 0);
-    part += min(max(quota[j], 0), nj);
+    part += min(max(quota_of<RATE>(quota, j, nj, num, den, cap), 0), nj);
   }
   const int sel_base = block_sum(part, scratch);
 
@@ -83,7 +99,10 @@ select_kernel(const float* __restrict__ score, const int32_t* __restrict__ off,
     if (tid == 0) flag_error(err, LRM_DEVERR_INDEX);
     n = 0;
   }
-  int q = quota[e];
+  int q = quota_of<RATE>(quota, e, n, num, den, cap);
+  if constexpr (RATE) {
+    if (tid == 0) quota[e] = q;
+  }
   if (q < 0 || q > n) {
     if (tid == 0) flag_error(err, LRM_DEVERR_QUOTA);
     q = min(max(q, 0), n);
@@ -208,22 +227,42 @@ select_kernel(const float* __restrict__ score, const int32_t* __restrict__ off,
 
 using namespace lrm;
 
-extern "C" lrm_status lrm_select_quota(const lrm_shape* s, const float* score,
-                                       const int32_t* off, const int32_t* quota,
-                                       uint8_t* keep, int32_t* sel_off, int32_t* sel_pos,
-                                       void* ws, size_t ws_bytes, void* stream) {
+template <bool RATE>
+static lrm_status select_entry(const lrm_shape* s, const float* score, const int32_t* off,
+                               int32_t* quota, int num, int den, int cap, uint8_t* keep,
+                               int32_t* sel_off, int32_t* sel_pos, void* ws, size_t ws_bytes,
+                               void* stream) {
   lrm_status st = check_shape(s);
   if (st != LRM_OK) return st;
   if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
   const int64_t N = (int64_t)s->T * s->K;
   if (!off || !quota || !sel_off) return LRM_ERR_INVALID_ARG;
   if (N > 0 && (!score || !keep || !sel_pos)) return LRM_ERR_INVALID_ARG;
+  if (RATE && (den <= 0 || num < 0 || num > den)) return LRM_ERR_INVALID_ARG;
   const int keys_cap = (int)std::min<int64_t>(std::max(s->T, 1), kSelSmemKeysMax);
   const size_t smem = (size_t)keys_cap * 4;
   if (smem > 48 * 1024)
-    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(select_kernel<RATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
-  launch_k(select_kernel, dim3(s->E), dim3(kSelThreads), smem, (cudaStream_t)stream, 
-      score, off, quota, s->E, keys_cap, keep, sel_off, sel_pos, error_word(ws));
+  launch_k(select_kernel<RATE>, dim3(s->E), dim3(kSelThreads), smem, (cudaStream_t)stream,
+           score, off, quota, num, den, cap, s->E, keys_cap, keep, sel_off, sel_pos,
+           error_word(ws));
   return launch_status();
+}
+
+extern "C" lrm_status lrm_select_quota(const lrm_shape* s, const float* score,
+                                       const int32_t* off, const int32_t* quota,
+                                       uint8_t* keep, int32_t* sel_off, int32_t* sel_pos,
+                                       void* ws, size_t ws_bytes, void* stream) {
+  return select_entry<false>(s, score, off, const_cast<int32_t*>(quota), 0, 1, 0, keep,
+                             sel_off, sel_pos, ws, ws_bytes, stream);
+}
+
+extern "C" lrm_status lrm_select_rate(const lrm_shape* s, const float* score,
+                                      const int32_t* off, int32_t num, int32_t den, int32_t cap,
+                                      int32_t* quota, uint8_t* keep, int32_t* sel_off,
+                                      int32_t* sel_pos, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  return select_entry<true>(s, score, off, quota, num, den, cap, keep, sel_off, sel_pos, ws,
+                            ws_bytes, stream);
 }

@@ -28,6 +28,7 @@ EXPORTS = (
     "lrm_dispatch_permute_noalloc", "lrm_selftest_wait_timeout", "lrm_score_variant",
     "lrm_gather_tokens", "lrm_expert_fc1_fwd", "lrm_expert_fc2_fwd", "lrm_combine",
     "lrm_expert_fwd_grouped", "lrm_expert_fc1_recompute", "lrm_expert_bwd_gathered",
+    "lrm_select_rate",
 )
 LRM_BWD_FC2_DGRAD, LRM_BWD_FC2_WGRAD, LRM_BWD_FC1_WGRAD = 1, 2, 4
 LRM_BWD_FC1_DGRAD, LRM_BWD_SCATTER_DX, LRM_BWD_ALL = 8, 16, 31
@@ -81,6 +82,7 @@ def _load():
         "lrm_expert_fwd_grouped": (i32, [sp] + [vp] * 13 + [vp, sz, vp]),
         "lrm_expert_fc1_recompute": (i32, [sp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "lrm_expert_bwd_gathered": (i32, [sp, i32] + [vp] * 18 + [vp, sz, vp]),
+        "lrm_select_rate": (i32, [sp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -290,3 +292,10 @@ def lrm_expert_bwd_gathered(shape, parts, sel_off, sel_pos, tok_c, w_gate, w_up,
         ctypes.byref(shape), parts, _p(sel_off), _p(sel_pos), _p(tok_c), _p(w_gate), _p(w_up),
         _p(w_down), _p(dy_c), _p(x), _p(ab), _p(phi), _p(inv), _p(row_of_pos), _p(dab_c),
         _p(dx_c), _p(dw_gate), _p(dw_up), _p(dw_down), _p(dx), _p(ws), ws_bytes, _s(stream)))
+
+
+def lrm_select_rate(shape, score, off, num, den, cap, quota, keep, sel_off, sel_pos, ws, ws_bytes,
+                    stream=None):
+    _check("lrm_select_rate", _lib.lrm_select_rate(
+        ctypes.byref(shape), _p(score), _p(off), num, den, cap, _p(quota), _p(keep), _p(sel_off),
+        _p(sel_pos), _p(ws), ws_bytes, _s(stream)))

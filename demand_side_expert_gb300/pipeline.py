@@ -126,6 +126,11 @@ class RecalibratedExpertBackward:
             lrm.lrm_score_variant(self.shape, metric, seed, g, phi, alpha, self.inv, self.score,
                                   self.ws, self.ws_bytes, stream)
 
+    def select_rate(self, num: int, den: int, cap: int = 0, stream=None):
+        """Quotas from the rate and the selection in one launch."""
+        lrm.lrm_select_rate(self.shape, self.score, self.off, num, den, cap, self.quota,
+                            self.keep, self.sel_off, self.sel_pos, self.ws, self.ws_bytes, stream)
+
     def select(self, stream=None):
         lrm.lrm_select_quota(self.shape, self.score, self.off, self.quota, self.keep,
                              self.sel_off, self.sel_pos, self.ws, self.ws_bytes, stream)
@@ -200,11 +205,13 @@ class RecalibratedExpertBackward:
         if gathered and ab is None:
             raise ValueError("the gathered backward reads saved [a | b]")
         self.dispatch(topk_idx, stream)
+        self.score_pairs(alpha, g, phi, stream, metric, seed)
         if quota is None:
-            self.quota_from_rate(rate[0], rate[1], cap, stream)
+            self.select_rate(rate[0], rate[1], cap, stream)
         else:
             self.quota.copy_(quota)
-        self.score_select_compact(alpha, x, g, ab, phi, stream, metric, seed, gathered)
+            self.select(stream)
+        self.compact(alpha, x, g, ab, phi, stream, gathered)
         if gathered:
             self.expert_bwd_gathered(x, ab, phi, w_gate, w_up, w_down, stream=stream)
             return

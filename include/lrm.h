@@ -419,6 +419,18 @@ lrm_status lrm_expert_bwd_gathered(const lrm_shape* shape, int32_t parts,
                                    float* dw_down, float* dx, void* ws, size_t ws_bytes,
                                    void* stream);
 
+/*
+ * lrm_quota_from_rate and lrm_select_quota in one launch: the quotas
+ * q_e = min(ceil(num/den * n_e), cap) (cap <= 0: none; exact integers, as
+ * lrm_quota_from_rate) are computed from off inside the selection and also
+ * written to quota [E] int32. Needs 0 <= num <= den, den > 0. Other
+ * arguments, outputs and error behaviour as lrm_select_quota.
+ */
+lrm_status lrm_select_rate(const lrm_shape* shape, const float* score, const int32_t* off,
+                           int32_t num, int32_t den, int32_t cap, int32_t* quota,
+                           uint8_t* keep, int32_t* sel_off, int32_t* sel_pos, void* ws,
+                           size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -548,3 +548,25 @@ def test_padding_rows_after_the_retained_rows_are_zero(dev):
     hi = min(M + 64, N)
     assert hi > M
     assert bool((pipe.dy_c[M:hi] == 0).all()) and bool((pipe.dab_c[M:hi] == 0).all())
+
+
+def test_select_rate_equals_quota_then_select(dev):
+    """The one-launch quota rule + selection gives the two-launch result."""
+    cfg = get_config("stress-e256", T=2048, D=256, H=128)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    for rate, cap in (((1, 2), 100), ((3, 5), 0), ((1, 1), 0), ((0, 1), 0)):
+        a, b = _pipe(cfg, dev), _pipe(cfg, dev)
+        for pipe in (a, b):
+            pipe.dispatch(inp["topk_idx"])
+            phi = pipe.to_dispatch_order(inp["phi_pair"])
+            pipe.score_pairs(inp["alpha"], inp["g"], phi)
+        a.quota_from_rate(rate[0], rate[1], cap)
+        a.select()
+        b.select_rate(rate[0], rate[1], cap)
+        torch.cuda.synchronize()
+        assert a.device_error() == 0 and b.device_error() == 0
+        N = cfg.N
+        M = a.retained_rows
+        for k in ("quota", "sel_off"):
+            assert torch.equal(getattr(a, k), getattr(b, k)), (rate, k)
+        assert torch.equal(a.keep[:N], b.keep[:N]) and torch.equal(a.sel_pos[:M], b.sel_pos[:M])
