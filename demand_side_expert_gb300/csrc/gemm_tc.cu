@@ -833,19 +833,28 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a_addr = su32(a_s), b_addr = su32(b_s);
+          // MN-major: 16 K-rows = 2 x 1024 B per step, 64-column boxes
+          // BOX_BYTES apart; K-major: 16 elements = 32 B per step
+          uint64_t ad[BK / 16], bd[BK / 16];
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
-            if (ks < nks) {
-              // MN-major: 16 K-rows = 2 x 1024 B per step, 64-column boxes
-              // BOX_BYTES apart; K-major: 16 elements = 32 B per step
-              const uint64_t ad = AMN ? sw128_desc(a_addr + ks * 2048, BOX_BYTES, 1024)
-                                      : sw128_desc(a_addr + ks * 32, 16, 1024);
-              const uint64_t bd = BMN ? sw128_desc(b_addr + ks * 2048, BOX_BYTES, 1024)
-                                      : sw128_desc(b_addr + ks * 32, 16, 1024);
-              const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
-              if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
-              else umma_bf16(d_tmem, ad, bd, idesc, accum);
-            }
+            ad[ks] = AMN ? sw128_desc(a_addr + ks * 2048, BOX_BYTES, 1024)
+                         : sw128_desc(a_addr + ks * 32, 16, 1024);
+            bd[ks] = BMN ? sw128_desc(b_addr + ks * 2048, BOX_BYTES, 1024)
+                         : sw128_desc(b_addr + ks * 32, 16, 1024);
+          }
+          auto issue = [&](int ks) {
+            const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
+            if constexpr (PAIR) umma_bf16_pair(d_tmem, ad[ks], bd[ks], idesc, accum);
+            else umma_bf16(d_tmem, ad[ks], bd[ks], idesc, accum);
+          };
+          if (nks == BK / 16) {  // a whole K block: the four MMAs back to back
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks) issue(ks);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+              if (ks < nks) issue(ks);
           }
           if constexpr (PAIR) umma_commit_pair(&empty[stage], 3);
           else umma_commit(&empty[stage]);
