@@ -223,12 +223,15 @@ def test_bad_expert_ids_and_quotas_are_flagged(dev):
 # ---------------------------------------------------------------------------
 # full-size layers, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
-def _full_size(name, rate, cap=0, sample_experts=3, sample_tokens=24, seed=None):
+def _full_size(name, rate, cap=0, sample_experts=3, sample_tokens=24, seed=None, gathered=True):
+    """A full-size layer in the launch configuration bench.py times (by
+    default the gathered backward): indices exhaustively, scores, expert
+    weight gradients and dx on sampled positions, experts and tokens."""
     cfg = get_config(name)
     dev = torch.device("cuda:0")
     inp = generate(cfg, device=dev, seed=seed)
     pipe = _pipe(cfg, dev)
-    run_gpu(pipe, inp, rate, cap)
+    ab_d, phi_d = run_gpu(pipe, inp, rate, cap, gathered=gathered)
     assert pipe.device_error() == 0
     nin = {k: (to_np(v) if torch.is_tensor(v) and k in ("topk_idx", "alpha") else v)
            for k, v in inp.items()}
@@ -239,15 +242,20 @@ def _full_size(name, rate, cap=0, sample_experts=3, sample_tokens=24, seed=None)
     rng = np.random.default_rng(0)
     # scores on sampled positions, one by one
     P = rng.choice(N, size=min(N, 4096), replace=False)
-    phi_s = to_np(pipe.to_dispatch_order(inp["phi_pair"])[torch.as_tensor(P, device=dev)])
+    phi_s = to_np(phi_d[torch.as_tensor(P, device=dev)])
     ref = oracle.score(to_np(inp["g"]), phi_s, nin["alpha"], perm[P], cfg.K)
     check_scores(to_np(pipe.score)[P], ref)
     keep, sel_off, sel_pos = check_selection(pipe, perm, off, qv)
     M = int(sel_off[-1])
-    assert np.array_equal(to_np(pipe.tok_c)[:M], perm[sel_pos] // cfg.K)
+    tok = perm[sel_pos] // cfg.K
+    assert np.array_equal(to_np(pipe.tok_c)[:M], tok)
     rop = np.full(N, -1)
     rop[sel_pos] = np.arange(M)
     assert np.array_equal(to_np(pipe.row_of_pos)[:N], rop)
+    # the retained rows' operands, taken from their sources by index (the
+    # gathered backward reads them in place)
+    sel_t = torch.as_tensor(sel_pos, device=dev)
+    tok_t = torch.as_tensor(tok, device=dev)
     # weight gradients of sampled experts (largest, smallest non-empty, random)
     m = np.diff(sel_off)
     nonempty = np.nonzero(m)[0]
@@ -261,8 +269,8 @@ def _full_size(name, rate, cap=0, sample_experts=3, sample_tokens=24, seed=None)
         lo, hi = int(sel_off[e]), int(sel_off[e + 1])
         rows = slice(lo, hi)
         b = oracle.expert_bwd(np.array([0, hi - lo]), *weights(e),
-                              to_np(pipe.dy_c[rows]), to_np(pipe.x_c[rows]),
-                              to_np(pipe.ab_c[rows]), to_np(pipe.phi_c[rows]))
+                              to_np(pipe.dy_c[rows]), to_np(inp["x"][tok_t[rows]]),
+                              to_np(ab_d[sel_t[rows]]), to_np(phi_d[sel_t[rows]]))
         for k in ("dw_gate", "dw_up", "dw_down"):
             err = rel_fro(to_np(getattr(pipe, k)[e]), b[k][0])
             assert err <= 2e-2, (name, e, k, err)
@@ -276,7 +284,7 @@ def _full_size(name, rate, cap=0, sample_experts=3, sample_tokens=24, seed=None)
             e = int(np.searchsorted(sel_off, j, side="right") - 1)
             _, dxc = oracle.expert_bwd_rows(np.array([0]), np.array([0, 1]), *weights(e),
                                             to_np(pipe.dy_c[j:j + 1]),
-                                            to_np(pipe.ab_c[j:j + 1]))
+                                            to_np(ab_d[sel_t[j:j + 1]]))
             want += dxc[0]
         got = to_np(pipe.dx[int(t)])
         assert np.linalg.norm(got - want) <= 2e-2 * max(np.linalg.norm(want), 1e-12), (name, t)
@@ -285,6 +293,10 @@ def _full_size(name, rate, cap=0, sample_experts=3, sample_tokens=24, seed=None)
 
 def test_full_size_qwen3_t4k(dev):
     _full_size("qwen3-30b-a3b-t4k", (3, 5))
+
+
+def test_full_size_qwen3_t4k_compacted(dev):
+    _full_size("qwen3-30b-a3b-t4k", (3, 5), gathered=False)
 
 
 def test_full_size_qwen3_t32k(dev):
