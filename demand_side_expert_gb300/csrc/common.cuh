@@ -11,9 +11,13 @@
 
 namespace lrm {
 
-constexpr size_t kWsHeaderBytes = 256;  // error word + reserved
+constexpr size_t kWsHeaderBytes = 256;  // error word, tile-queue counters, reserved
+constexpr int kWsHeaderWords = 8;        // words the header clear zeroes
 
 inline int32_t* error_word(void* ws) { return static_cast<int32_t*>(ws); }
+// The weight-gradient products' tile queue: next position, CTAs done, tiles
+// handed out (words 4..6 of the header, after the error word).
+inline int32_t* queue_words(int32_t* err) { return err ? err + 4 : nullptr; }
 
 inline bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;

@@ -308,7 +308,9 @@ __global__ void quota_kernel(const int32_t* __restrict__ counts, int E, int num,
   quota[e] = (int32_t)q;
 }
 
-__global__ void clear_word_kernel(int32_t* w) { *w = 0; }
+__global__ void clear_header_kernel(int32_t* w) {
+  if (threadIdx.x < kWsHeaderWords) w[threadIdx.x] = 0;
+}
 
 }  // namespace lrm
 
@@ -332,7 +334,7 @@ extern "C" const char* lrm_status_string(lrm_status s) {
 
 extern "C" lrm_status lrm_clear_device_error(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < kWsHeaderBytes) return LRM_ERR_WORKSPACE;
-  clear_word_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(error_word(ws));
+  clear_header_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(error_word(ws));
   return launch_status();
 }
 

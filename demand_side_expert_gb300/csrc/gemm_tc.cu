@@ -62,6 +62,12 @@ constexpr int MAX_STAGES = 6;  // operand ring depth (runtime: as deep as shared
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each half the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kGatherWarps = 4;  // weight-gradient products: A rows gathered by index
+// Weight-gradient products on single CTAs take their tiles from a queue in
+// the workspace header (1) instead of a fixed deal (0).
+#ifndef LRM_TC_WG_QUEUE
+#define LRM_TC_WG_QUEUE 1
+#endif
+constexpr int kTQ = 8;  // tile ids in flight between the copy lane and the other roles
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 // B rows a CTA loads: all BN columns alone, half of them in a CTA pair
 template <bool PAIR>
@@ -107,6 +113,7 @@ struct Params {
   int a_src_rows, a_src_cols;
   int ab_src_rows;  // rows of the [a | b] source (bound for ab_rows)
   int32_t* err;
+  int32_t* queue;  // weight-gradient tile queue: [next position, CTAs done, tiles handed out]
 };
 
 // ----------------------------------------------------------------------------
@@ -551,11 +558,14 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   uint64_t* tfull = bars + 2 * MAX_STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tq_full = drain + 1;     // [kTQ] tile id published
+  uint64_t* tq_empty = tq_full + kTQ;  // [kTQ] tile id read by every consumer warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq_empty + kTQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bad_flag = const_cast<int*>(abort_flag) + 1;
   int* goff = bad_flag + 1;          // [E+1]
   int* tab = goff + p.E + 1;         // dgrad: tpre[E+1]; wgrad: order[E]
+  int* tq_id = tab + p.E + 1;        // [kTQ]
   const CUtensorMap* mapA = &maps.a;
   const CUtensorMap* mapB = &maps.b;
   const CUtensorMap* mapB2 = &maps.b2;
@@ -566,6 +576,9 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   const bool leader = rank == 0;
   const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const bool queued = WG && !PAIR && LRM_TC_WG_QUEUE && p.queue != nullptr;
+  // warps that read every tile id: MMA, epilogue, and the gather warps at work
+  const int gathering = (NG > 0 && p.a_rows && !p.selftest) ? min(NG, STAGES) : 0;
 
   // --- set-up that reads nothing a kernel writes: barriers, TMEM, maps ----
   if (tid == 0) {
@@ -583,6 +596,10 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       mbar_init(&tempty[a], kEpiWarps * (PAIR ? 2 : 1));
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kTQ; ++i) {
+      mbar_init(&tq_full[i], 1);
+      mbar_init(&tq_empty[i], 1 + kEpiWarps + gathering);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0 && !p.selftest) {
@@ -710,10 +727,32 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     __syncwarp();
   };
 
-  // Tile r of this unit (CTA or CTA pair): serpentine over the units, so that
-  // with tiles sorted longest first (weight-gradient products) every unit's
-  // total stays close to the mean. Every role walks the same sequence.
-  auto tile_of = [&](int r) { return r * units + ((r & 1) ? units - 1 - unit : unit); };
+  // The tile sequence every role of this CTA walks, one call per tile r =
+  // 0, 1, ...; a value >= sc.total ends it.
+  //
+  // Fixed deal: tile r of this unit (CTA or CTA pair), serpentine over the
+  // units, so that with tiles sorted longest first (weight-gradient products)
+  // every unit's total stays close to the mean.
+  //
+  // Queue (weight-gradient products on single CTAs): the copy lane takes the
+  // next position of the longest-first list with an atomic add and publishes
+  // the tile id in a ring of kTQ slots that the MMA, epilogue and gather warps
+  // read in order. A tile's cost varies with its group (long groups: bound by
+  // the tensor pipe; short ones and empty ones: by the fp32 stores) and with
+  // the SM, so a fixed deal ends unevenly (CTAs measured up to 20% apart);
+  // taking tiles as the CTA frees up ends within about one tile.
+  auto tile_of = [&](int r) -> int {
+    if (queued) {
+      const int slot = r % kTQ;
+      if (!warp_wait(&tq_full[slot], (uint32_t)(r / kTQ) & 1u, abort_flag, p.err, p.wait_ns))
+        return sc.total;
+      const int id = *reinterpret_cast<volatile int*>(&tq_id[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tq_empty[slot]);
+      return id;
+    }
+    return r * units + ((r & 1) ? units - 1 - unit : unit);
+  };
 
   if (warp == 0) {
     // ===================== TMA producer =====================
@@ -722,7 +761,31 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       uint32_t issued_mask = 0, issued_parity = 0;
       uint32_t tail_parity = 0;  // odd CTA of a pair: its own full barriers flip only on tails
       bool stop = false;
-      for (int ri = 0, tau = tile_of(0); tau < sc.total && !stop; tau = tile_of(++ri)) {
+      int handed = 0;        // tiles this CTA took from the queue
+      bool drained = false;  // the queue ran out
+      // the position of the next tile, taken one tile ahead so that the
+      // atomic's round trip overlaps the current tile's copies
+      int ahead = queued ? atomicAdd(p.queue, 1) : 0;
+      auto next = [&](int r) -> int {
+        if (!queued) return tile_of(r);
+        const int slot = r % kTQ;
+        int tau = sc.total;
+        if (mbar_wait(&tq_empty[slot], ((uint32_t)(r / kTQ) & 1u) ^ 1u, abort_flag, p.err,
+                      p.wait_ns) &&
+            !drained) {
+          if (ahead >= 0 && ahead < sc.total) {
+            tau = ahead;
+            ++handed;
+            ahead = atomicAdd(p.queue, 1);
+          } else {
+            drained = true;
+          }
+        }
+        tq_id[slot] = tau;  // published by the arrival (release)
+        mbar_arrive(&tq_full[slot]);
+        return tau;
+      };
+      for (int ri = 0, tau = next(0); tau < sc.total; tau = stop ? sc.total : next(++ri)) {
         const Tile t = decode<MODE>(sc, tau, rank);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_ns)) {
@@ -803,6 +866,22 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       // (in a pair the even CTA's barriers also count the odd CTA's bytes)
       for (int s = 0; s < STAGES; ++s)
         if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_parity >> s) & 1u);
+      if (queued) {
+        // this CTA takes no more tiles: the last CTA to get here checks that
+        // every tile was handed out once and rewinds the queue for the next
+        // launch (which reads it only after this grid has completed)
+        atomicAdd(p.queue + 2, handed);
+        __threadfence();
+        const int prev = atomicAdd(p.queue + 1, 1);
+        if (prev < 0 || prev >= (int)gridDim.x) flag_error(p.err, LRM_DEVERR_QUEUE);
+        if (prev == (int)gridDim.x - 1) {
+          __threadfence();
+          if (atomicAdd(p.queue + 2, 0) != sc.total) flag_error(p.err, LRM_DEVERR_QUEUE);
+          atomicExch(p.queue, 0);
+          atomicExch(p.queue + 1, 0);
+          atomicExch(p.queue + 2, 0);
+        }
+      }
     }
   } else if (warp == 1 && (!PAIR || leader)) {
     // ===================== MMA issuer =====================
@@ -1240,7 +1319,7 @@ constexpr size_t kSmemLimit = 232448;  // 227 KB per block
 
 static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs) {
   return 1024 + (size_t)stages * stage_bytes + (size_t)kEpiWarps * stage_bufs * STAGING_BYTES +
-         8 * (2 * MAX_STAGES + 5) + 16 + (size_t)(2 * (E + 1) + 2) * 4;
+         8 * (2 * MAX_STAGES + 5 + 2 * kTQ) + 16 + (size_t)(2 * (E + 1) + 2 + kTQ) * 4;
 }
 
 // Staging blocks per epilogue warp for fp32 outputs (two keep twice the store
@@ -1354,6 +1433,7 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   p.a_src_rows = p.a_src_cols = 0;
   p.ab_src_rows = (int)N;
   p.err = a.err;
+  p.queue = queue_words(a.err);
   lrm_status st = LRM_OK;
   const bool gathered = a.sel_pos != nullptr;
   if (gathered && !a.tok_c) return LRM_ERR_INVALID_ARG;
@@ -1461,6 +1541,7 @@ lrm_status launch_fwd_tc(const FwdArgs& a, unsigned parts) {
   p.n_rows = (int)N;
   p.sel_off = a.off;
   p.err = a.err;
+  p.queue = queue_words(a.err);
   lrm_status st = LRM_OK;
   // upper bound of the tile count: every group may end in a partial tile
   auto tiles = [&](int tm, int ntn) { return ((int64_t)N / tm + E) * ntn; };

@@ -17,6 +17,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblrm.so"
 LRM_OK, LRM_ERR_INVALID_ARG, LRM_ERR_UNSUPPORTED, LRM_ERR_WORKSPACE, LRM_ERR_CUDA = range(5)
 LRM_F32, LRM_BF16 = 0, 1
 LRM_DEVERR_EXPERT_ID, LRM_DEVERR_QUOTA, LRM_DEVERR_INDEX, LRM_DEVERR_TIMEOUT = 1, 2, 4, 8
+LRM_DEVERR_QUEUE = 16
 
 # Every symbol include/lrm.h declares.
 EXPORTS = (

@@ -36,8 +36,12 @@
  *    bytes of the caller's workspace, and the call returns LRM_OK; read the
  *    word with lrm_get_device_error.
  *  - ws / ws_bytes: caller-owned device workspace of at least
- *    lrm_workspace_bytes(shape) bytes, 256-byte aligned. Clear its error word
- *    once with lrm_clear_device_error before first use.
+ *    lrm_workspace_bytes(shape) bytes, 256-byte aligned. Its first 256 bytes
+ *    are a header: the device error word and the tile-queue counters of the
+ *    weight-gradient products, which every such launch leaves at zero for
+ *    the next one. Zero the header once with lrm_clear_device_error before
+ *    first use, and let one workspace serve one stream at a time (two
+ *    weight-gradient launches in flight together would share the queue).
  */
 #ifndef LRM_H_
 #define LRM_H_
@@ -70,11 +74,16 @@ typedef struct lrm_shape {
 #define LRM_DEVERR_QUOTA 2     /* quota outside [0,n_e]: clamped           */
 #define LRM_DEVERR_INDEX 4     /* inv / perm / sel_pos out of range: row skipped */
 #define LRM_DEVERR_TIMEOUT 8   /* a GEMM pipeline wait gave up: outputs invalid */
+#define LRM_DEVERR_QUEUE 16    /* a weight-gradient tile queue did not hand out
+                                  every tile once (header not zeroed before first
+                                  use, or shared by concurrent launches): outputs
+                                  invalid; the queue is rewound for the next call */
 
 /* Bytes of workspace every call of this shape needs (host only, pure). */
 size_t lrm_workspace_bytes(const lrm_shape* shape);
 
-/* Zero the device error word (first 4 bytes of ws). Async on stream. */
+/* Zero the workspace header (the device error word in its first 4 bytes and
+ * the tile-queue counters). Async on stream. */
 lrm_status lrm_clear_device_error(void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, then copy the device error word into *code_out. */

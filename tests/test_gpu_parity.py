@@ -193,6 +193,31 @@ def test_deterministic_repeats(dev):
                 assert torch.equal(a, b)
 
 
+def test_weight_gradient_queue_flags_a_bad_header_and_rewinds(dev):
+    """The weight-gradient products take their tiles from a queue in the
+    workspace header that every launch leaves at zero. A queue that does not
+    start at zero (a header never cleared) skips tiles: the launch flags
+    LRM_DEVERR_QUEUE and rewinds the queue, and the next step is exact again."""
+    from demand_side_expert_gb300 import lrm
+    cfg = get_config("qwen3-30b-a3b-t4k", T=512, D=256, H=128, E=8, K=4)
+    inp = _to(generate(cfg, device="cpu"), dev)
+    pipe = _pipe(cfg, dev)
+    words = pipe.ws.view(torch.int32)
+    run_gpu(pipe, inp, (1, 2), gathered=True)
+    assert pipe.device_error() == 0
+    assert words[4:7].tolist() == [0, 0, 0]
+    ref = [getattr(pipe, k).clone() for k in ("dw_gate", "dw_up", "dw_down", "dx")]
+    words[4] = 3  # the queue would start past three tiles
+    run_gpu(pipe, inp, (1, 2), gathered=True)
+    assert pipe.device_error() & lrm.LRM_DEVERR_QUEUE
+    assert words[4:7].tolist() == [0, 0, 0]
+    pipe.clear_device_error()
+    run_gpu(pipe, inp, (1, 2), gathered=True)
+    assert pipe.device_error() == 0
+    for k, r in zip(("dw_gate", "dw_up", "dw_down", "dx"), ref):
+        assert torch.equal(getattr(pipe, k), r), k
+
+
 def test_bad_expert_ids_and_quotas_are_flagged(dev):
     from demand_side_expert_gb300 import lrm
     cfg = get_config("qwen3-30b-a3b-t4k", T=64, D=128, H=64, E=8, K=2)
