@@ -55,6 +55,13 @@ FWD_KERNEL_NAMES = {
 }
 
 
+def segment_kernels(seg: str, N: int, fwd: bool = False) -> str:
+    """Kernel name(s) of a segment as the launch list shows them."""
+    if seg == "dispatch" and N > FUSED_DISPATCH_MAX_PAIRS:
+        return "dispatch_hist_kernel + dispatch_scan_kernel + dispatch_scatter_kernel"
+    return (FWD_KERNEL_NAMES if fwd else KERNEL_NAMES)[seg]
+
+
 def kernels_per_step(N: int) -> int:
     """Launches of one step: dispatch (1 or 3), score, select (with the quota
     rule), compact, four grouped GEMMs, dx scatter."""
@@ -90,6 +97,10 @@ def parse_args():
                     "products read the others in place")
     ap.add_argument("--no-other-backward", action="store_true",
                     help="skip timing the step with the other --backward variant")
+    ap.add_argument("--index-sweep", action="store_true",
+                    help="supplementary: time the dispatch permutation and the selection "
+                         "(with the quota rule) alone over routed-pair counts 2^15..2^22 "
+                         "and print one JSON line; the headline run is not made")
     ap.add_argument("--no-recompute", action="store_true",
                     help="skip the timing of the backward step that recomputes [a | b]")
     return ap.parse_args()
@@ -396,7 +407,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     kernels = {}
     for s in SEGMENTS:
         ms = statistics.mean(seg_ms[s])
-        k = {"ms": round(ms, 4), "kernels": KERNEL_NAMES[s],
+        k = {"ms": round(ms, 4), "kernels": segment_kernels(s, cfg.N),
              "gbs": round(alg[s]["bytes"] / (ms * 1e-3) / 1e9, 1)}
         if "flops" in alg[s]:
             k["tflops"] = round(alg[s]["flops"] / (ms * 1e-3) / 1e12, 1)
@@ -582,7 +593,7 @@ def run_forward(pipe, inp, cfg, flush, stream, args):
     peaks = load_peaks()
     kernels = {}
     for s in FWD_SEGMENTS:
-        k = {"ms": round(seg[s], 4), "kernels": FWD_KERNEL_NAMES[s],
+        k = {"ms": round(seg[s], 4), "kernels": segment_kernels(s, cfg.N, fwd=True),
              "gbs": round(alg[s]["bytes"] / (seg[s] * 1e-3) / 1e9, 1)}
         if "flops" in alg[s]:
             k["tflops"] = round(alg[s]["flops"] / (seg[s] * 1e-3) / 1e12, 1)
@@ -768,8 +779,73 @@ def run_reference(args, rank: int):
     }
 
 
+def run_index_sweep(args):
+    """The two latency-bound index steps at growing N = T*K (K = 8, E = 128, zipf-skewed
+    routing, rho = 1/2, random scores), each timed alone with CUDA events (L2 flushed
+    before every launch). GB/s counts the algorithmic bytes: dispatch 4N + 16N + 8E,
+    selection 4N + N + 4M + 16E."""
+    import torch
+    from demand_side_expert_gb300 import lrm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    E, K, num, den = 128, 8, 1, 2
+    gen = torch.Generator(device=dev).manual_seed(0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    probs = 1.0 / torch.arange(1, E + 1, device=dev, dtype=torch.float64) ** 1.2
+    points = []
+    for log_n in range(15, 23):
+        N = 1 << log_n
+        T = N // K
+        shape = lrm.make_shape(T, 64, 64, E, K, lrm.LRM_BF16)
+        ws_bytes = lrm.lrm_workspace_bytes(shape)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        topk = torch.multinomial(probs.float().expand(T, E), K, replacement=False,
+                                 generator=gen).to(torch.int32)
+        i32 = dict(dtype=torch.int32, device=dev)
+        perm, inv = torch.empty(N, **i32), torch.empty(N, **i32)
+        counts, off, quota = torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(E, **i32)
+        score = torch.rand(N, generator=gen, device=dev)
+        keep = torch.empty(N, dtype=torch.uint8, device=dev)
+        sel_off, sel_pos = torch.empty(E + 1, **i32), torch.empty(N, **i32)
+        calls = {
+            "dispatch": lambda: lrm.lrm_dispatch_permute(shape, topk, perm, inv, counts, off,
+                                                         ws, ws_bytes, None),
+            "select": lambda: lrm.lrm_select_rate(shape, score, off, num, den, 0, quota, keep,
+                                                  sel_off, sel_pos, ws, ws_bytes, None),
+        }
+        point = {"N": N}
+        for name, fn in calls.items():
+            for _ in range(max(args.warmup, 3)):
+                fn()
+            times = []
+            for _ in range(20):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            point[name + "_us"] = round(statistics.median(times) * 1e3, 2)
+        M = int(sel_off[-1].item())
+        point["M"] = M
+        point["dispatch_gbs"] = round((20 * N + 8 * E) / (point["dispatch_us"] * 1e3), 1)
+        point["select_gbs"] = round((5 * N + 4 * M + 16 * E) / (point["select_us"] * 1e3), 1)
+        code = lrm.lrm_get_device_error(ws, ws_bytes)
+        if code:
+            raise RuntimeError(f"device error word {code} at N = {N}")
+        points.append(point)
+    return {"metric": "index steps alone over routed pairs N (supplementary sweep)",
+            "unit": "GB/s", "data": "synthetic (zipf 1.2 routing over 128 experts, K = 8, "
+            "rho = 1/2, uniform random scores)", "points": points}
+
+
 def main():
     args = parse_args()
+    if args.index_sweep:
+        print(json.dumps(run_index_sweep(args)), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -5,7 +5,9 @@
 // ("Least-Loaded Expert Parallelism", Sec. 2.1 re-index and Alg. 4 sort of
 // the flattened indices; LRMoE Alg. 1 counts N_e). Up to 2^20 pairs it is one
 // launch of one 8-CTA cluster (dispatch_fused_kernel below); beyond that,
-// three launches with no inter-CTA waiting:
+// three launches with no inter-CTA waiting (with 128 experts the three
+// launches are faster from 2^17 pairs on, with 256 experts slower at 2^18,
+// measured on one GB300):
 //   1. per-chunk histogram (each CTA owns kChunk consecutive pairs),
 //   2. one CTA scans counts -> off and chunk bases (expert-major),
 //   3. each CTA replays its chunk warp by warp; inside a warp, lanes that
@@ -178,7 +180,10 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int n
 constexpr int kFusedCtas = 8;
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr int64_t kFusedMaxPairs = 1 << 20;
+#ifndef LRM_DISPATCH_FUSED_MAX
+#define LRM_DISPATCH_FUSED_MAX (1 << 20)
+#endif
+constexpr int64_t kFusedMaxPairs = LRM_DISPATCH_FUSED_MAX;
 
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");

@@ -193,6 +193,19 @@ def test_deterministic_repeats(dev):
                 assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("T", [131072, 131073])
+def test_dispatch_either_side_of_the_single_launch_limit(dev, T):
+    """2^20 routed pairs take the one-cluster launch, 2^20 + 8 the three launches;
+    both are the oracle's stable counting sort, bit for bit."""
+    cfg = get_config("qwen3-30b-a3b-t4k", T=T, D=64, H=64)
+    inp = generate(cfg, device="cpu")
+    pipe = _pipe(cfg, dev)
+    pipe.dispatch(inp["topk_idx"].to(dev))
+    torch.cuda.synchronize()
+    assert pipe.device_error() == 0
+    check_dispatch(pipe, inp["topk_idx"].numpy(), cfg.E)
+
+
 def test_weight_gradient_queue_flags_a_bad_header_and_rewinds(dev):
     """The weight-gradient products take their tiles from a queue in the
     workspace header that every launch leaves at zero. A queue that does not
