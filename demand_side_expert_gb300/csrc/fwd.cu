@@ -40,37 +40,40 @@ gather_tokens_kernel(const int32_t* __restrict__ perm, const uint4* __restrict__
 }
 
 // out[t] = sum_k alpha[t,k] * y[inv[t*K+k]], slots in ascending k, FP32.
-// One warp per token; lane k holds slot k's position and weight.
+// A CTA per token: its warps split the D columns, and in every warp lane k
+// holds slot k's position and weight (so a token's rows are read by 256
+// threads at once, and 8 tokens per SM are in flight instead of one warp's
+// worth). Each output element sums its slots in slot order.
+constexpr int kCombineWarps = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(32 * kCombineWarps)
 combine_kernel(const T* __restrict__ y, const float* __restrict__ alpha,
                const int32_t* __restrict__ inv, float* __restrict__ out, int ntok, int D, int K,
                int32_t* err) {
   pdl_begin();  // predecessor complete before any global access
   constexpr int V = Vec16<T>::kElems;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t N = (int64_t)ntok * K;
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t t = warp; t < ntok; t += nwarps) {
+  for (int64_t t = blockIdx.x; t < ntok; t += gridDim.x) {
     int pos = -1;
-    float w = 0.f;
+    float wt = 0.f;
     if (lane < K) {
       const int q = inv[t * K + lane];
       if (q >= 0 && q < N) {
         pos = q;
-        w = alpha[t * K + lane];
-      } else {
+        wt = alpha[t * K + lane];
+      } else if (w == 0) {
         flag_error(err, LRM_DEVERR_INDEX);
       }
     }
-    for (int c = lane * V; c < D; c += 32 * V) {
+    for (int c = (w * 32 + lane) * V; c < D; c += 32 * kCombineWarps * V) {
       float acc[V];
 #pragma unroll
       for (int u = 0; u < V; ++u) acc[u] = 0.f;
       for (int k = 0; k < K; ++k) {
         const int r = __shfl_sync(0xffffffffu, pos, k);
-        const float a = __shfl_sync(0xffffffffu, w, k);
+        const float a = __shfl_sync(0xffffffffu, wt, k);
         if (r >= 0) {
           float f[V];
           Vec16<T>::unpack(ld_stream(y + (int64_t)r * D + c), f);
@@ -103,12 +106,13 @@ static lrm_status launch_gather(const lrm_shape* s, const int32_t* perm, const v
 static lrm_status launch_combine(const lrm_shape* s, const void* y, const float* alpha,
                                  const int32_t* inv, float* out, int32_t* err, cudaStream_t cs) {
   if (s->T == 0) return LRM_OK;
+  const int blocks = (int)std::min<int64_t>(s->T, (int64_t)num_sms() * 64);
   if (s->dtype == LRM_BF16)
-    launch_k(combine_kernel<__nv_bfloat16>, dim3(warp_grid(s->T)), dim3(256), 0, cs, 
-        (const __nv_bfloat16*)y, alpha, inv, out, s->T, s->D, s->K, err);
+    launch_k(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(32 * kCombineWarps), 0, cs,
+             (const __nv_bfloat16*)y, alpha, inv, out, s->T, s->D, s->K, err);
   else
-    launch_k(combine_kernel<float>, dim3(warp_grid(s->T)), dim3(256), 0, cs, (const float*)y, alpha, inv, out,
-                                                           s->T, s->D, s->K, err);
+    launch_k(combine_kernel<float>, dim3(blocks), dim3(32 * kCombineWarps), 0, cs,
+             (const float*)y, alpha, inv, out, s->T, s->D, s->K, err);
   return launch_status();
 }
 
