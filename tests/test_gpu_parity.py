@@ -119,6 +119,24 @@ def test_explicit_quotas_and_extremes(dev):
     full_parity(cfg, dev, (1, 1), quota=quota.astype(np.int32))
 
 
+@pytest.mark.parametrize("over,rate", [
+    (dict(T=300, D=128, H=64, E=6, K=1), (1, 2)),   # top-1 routing
+    (dict(T=200, D=128, H=64, E=1, K=1), (3, 5)),   # one expert holding every token
+    (dict(T=1, D=128, H=64, E=8, K=2), (1, 1)),     # a single token
+    (dict(T=1, D=128, H=64, E=8, K=2), (1, 2)),     # a single token, half its pairs
+])
+def test_degenerate_routings(dev, over, rate):
+    full_parity(get_config("qwen3-30b-a3b-t4k", **over), dev, rate)
+
+
+@pytest.mark.parametrize("over,rate", [
+    (dict(T=300, D=128, H=64, E=6, K=1), (1, 2)),
+    (dict(T=200, D=128, H=64, E=1, K=1), (3, 5)),
+])
+def test_degenerate_routings_gathered(dev, over, rate):
+    full_parity(get_config("qwen3-30b-a3b-t4k", **over), dev, rate, gathered=True)
+
+
 def test_zero_retention(dev):
     cfg = get_config("qwen3-30b-a3b-t4k", T=256, D=128, H=64, E=8, K=2)
     pipe, _ = full_parity(cfg, dev, (0, 1))
