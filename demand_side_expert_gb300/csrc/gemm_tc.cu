@@ -800,9 +800,16 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           const bool to_leader = PAIR && !leader && !tailz;
           const uint32_t bar_cl = to_leader ? mapa(&full[stage], 0) : 0u;
           const bool gathered_a = NG > 0 && p.a_rows != nullptr;  // A copied by the gather warps
+          // A row tile of a pair whose odd CTA holds no row of the group (a
+          // group of at most BM rows): the odd CTA's accumulator rows are
+          // never stored, so its A box is not copied (the MMA reads whatever
+          // that stage held: it only feeds those discarded rows)
+          const bool odd_idle = !WG && PAIR && t.valid <= BM;
           if (!to_leader)
-            mbar_expect_tx(&full[stage], gathered_a ? STB - A_BYTES
-                                         : (PAIR && leader && !tailz) ? 2 * STB : STB);
+            mbar_expect_tx(&full[stage],
+                           gathered_a                       ? STB - A_BYTES
+                           : (PAIR && leader && !tailz)     ? 2 * STB - (odd_idle ? A_BYTES : 0)
+                                                            : STB);
           auto load2 = [&](uint8_t* dst, const CUtensorMap* m, int x, int y) {
             if (to_leader) tma_load_2d_pair(dst, m, bar_cl, x, y);
             else tma_load_2d(dst, m, &full[stage], x, y);
@@ -813,16 +820,16 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           };
           const int nb0 = t.n0 + rank * BNL;  // first B row (N) this CTA loads
           if constexpr (MODE == kG1) {
-            load2(a_s, mapA, kb * BK, t.cm0);
+            if (leader || !odd_idle) load2(a_s, mapA, kb * BK, t.cm0);
             load3(b_s, mapB, kb * BK, nb0, t.e);
           } else if constexpr (MODE == kG4) {
-            load2(a_s, mapA, kb * BK, t.cm0);
+            if (leader || !odd_idle) load2(a_s, mapA, kb * BK, t.cm0);
             const int hb = p.H / BK;
             if (kb < hb) load3(b_s, mapB, kb * BK, nb0, t.e);
             else load3(b_s, mapB2, (kb - hb) * BK, nb0, t.e);
           } else if constexpr (MODE == kF1) {
             // tile columns [0, 128): gate h0.., [128, 256): up h0..; 64 x 64 boxes
-            load2(a_s, mapA, kb * BK, t.cm0);
+            if (leader || !odd_idle) load2(a_s, mapA, kb * BK, t.cm0);
             const int h0 = t.n0 / 2;
 #pragma unroll
             for (int i = 0; i < BNL / 64; ++i) {
@@ -831,7 +838,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
                     kb * BK, t.e);
             }
           } else if constexpr (MODE == kF2) {
-            load2(a_s, mapA, kb * BK, t.cm0);
+            if (leader || !odd_idle) load2(a_s, mapA, kb * BK, t.cm0);
 #pragma unroll
             for (int i = 0; i < BNL / 64; ++i)
               load3(b_s + i * BOX_BYTES, mapB, nb0 + 64 * i, kb * BK, t.e);
