@@ -22,9 +22,14 @@
 // the compacted retained rows (groups from sel_off, phi not written) is the
 // retained-only recompute of [a | b] in the backward.
 //
-// Kernel shape (one CTA per SM, persistent over a device-computed tile list):
-//   warp 0    TMA producer: 128x64 A and 256x64 B tiles, 128-byte swizzle,
-//             4-stage ring of 48 KB stages guarded by mbarriers;
+// Kernel shape (one CTA per SM, persistent over a device-computed tile list;
+// the data-gradient and forward products run on CTA pairs, 256-row tiles
+// with tcgen05.mma.cta_group::2, each CTA reading half of the B tile; the
+// weight-gradient products on single CTAs that take their tiles from a queue
+// in the workspace header):
+//   warp 0    TMA producer: 128x64 A and 256x64 (pair: 128x64) B tiles,
+//             128-byte swizzle, a ring of 48 KB (pair: 32 KB) stages, as deep
+//             as shared memory allows (at most 6), guarded by mbarriers;
 //   warp 1    allocates 512 TMEM columns, one elected lane issues
 //             tcgen05.mma (M=128, N=256, K=16) into one of two 256-column
 //             accumulators; tcgen05.commit frees smem stages and hands
