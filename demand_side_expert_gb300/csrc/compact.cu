@@ -18,17 +18,8 @@
 
 namespace lrm {
 
-// At most 64 registers per thread, so that four CTAs (32 warps) fit per SM:
-// each warp's rows wait on a chain of dependent loads (sel_pos, perm, alpha,
-// the g row), and more warps hide more of it. Unbounded the kernel takes 80
-// registers and three CTAs per SM (the default layer's compaction: 29 us
-// against 25 us with the bound, despite a few spilled bytes); bounded to six
-// CTAs it spills heavily and takes 40 us.
-#ifndef LRM_COMPACT_MIN_CTAS
-#define LRM_COMPACT_MIN_CTAS 4
-#endif
 template <typename T>
-__global__ void __launch_bounds__(256, LRM_COMPACT_MIN_CTAS)
+__global__ void __launch_bounds__(256)
 compact_kernel(const int32_t* __restrict__ perm, const uint8_t* __restrict__ keep,
                const int32_t* __restrict__ sel_off, const int32_t* __restrict__ sel_pos,
                const float* __restrict__ alpha, const T* __restrict__ x,
