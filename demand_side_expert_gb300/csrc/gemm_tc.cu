@@ -18,7 +18,10 @@
 //       128 gate columns and the same 128 up columns, so every thread has the
 //       a and b of its outputs.
 //   F2  y = phi W_down[e]   [n_e x D] (bf16).
-// Both read the weights in their stored layout (MN-major B operands). F1 over
+// Both read the weights in their stored layout (MN-major B operands) and
+// write an epilogue warp's 32 x 32 output blocks that lie inside the group
+// through shared memory with TMA stores (a block crossing the group's end
+// takes 16-byte row stores). F1 over
 // the compacted retained rows (groups from sel_off, phi not written) is the
 // retained-only recompute of [a | b] in the backward.
 //
@@ -71,6 +74,11 @@ constexpr int kGatherWarps = 4;  // weight-gradient products: A rows gathered by
 // the workspace header (1) instead of a fixed deal (0).
 #ifndef LRM_TC_WG_QUEUE
 #define LRM_TC_WG_QUEUE 1
+#endif
+// forward products: full 32-row blocks of their bf16 outputs through staged
+// TMA stores (1) instead of 16-byte row stores (0)
+#ifndef LRM_TC_FWD_STAGED
+#define LRM_TC_FWD_STAGED 1
 #endif
 constexpr int kTQ = 8;  // tile ids in flight between the copy lane and the other roles
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
@@ -1192,6 +1200,9 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         const bool rv = row_local < t.cvalid;
         const int64_t j = (int64_t)t.cm0 + row_local;
         const int hbase = ((warp - 2) >> 2) * (BN / 4);
+        // the warp's 32 rows inside the group (warp-uniform): a, b and phi go
+        // out as 32 x 32 blocks (64-byte swizzle) through TMA stores
+        const bool whole = LRM_TC_FWD_STAGED && q * 32 + 32 <= t.cvalid;
 #pragma unroll 1
         for (int cc = 0; cc < BN / 4; cc += 32) {
           const int hl = hbase + cc;
@@ -1200,7 +1211,42 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           tmem_ld32(taddr + BN / 2 + hl, rb);
           tmem_ld_wait();
           const int h = t.n0 / 2 + hl;
-          if (rv && h < p.H) {
+          if (whole && h < p.H) {
+            uint4 av[4], bv[4], fv[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float a[8], b[8], f[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                a[u] = __uint_as_float(ra[8 * v + u]);
+                b[u] = __uint_as_float(rb[8 * v + u]);
+                f[u] = a[u] * __fdividef(1.0f, 1.0f + __expf(-a[u])) * b[u];
+              }
+              av[v] = Vec16<__nv_bfloat16>::pack(a);
+              bv[v] = Vec16<__nv_bfloat16>::pack(b);
+              fv[v] = Vec16<__nv_bfloat16>::pack(f);
+            }
+            // one set of blocks per warp: a second set costs a ring stage
+            // and measured slower
+            uint8_t* sb = wst;
+            if (lane == 0) bulk_wait_read(0);
+            __syncwarp();
+            const int sw = (lane >> 1) & 3;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              *reinterpret_cast<uint4*>(sb + lane * 64 + ((v ^ sw) << 4)) = av[v];
+              *reinterpret_cast<uint4*>(sb + 2048 + lane * 64 + ((v ^ sw) << 4)) = bv[v];
+              if (p.ob1) *reinterpret_cast<uint4*>(sb + 4096 + lane * 64 + ((v ^ sw) << 4)) = fv[v];
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&maps.o1, sb, h, t.cm0 + q * 32);
+              tma_store_2d(&maps.o1, sb + 2048, p.H + h, t.cm0 + q * 32);
+              if (p.ob1) tma_store_2d(&maps.o2, sb + 4096, h, t.cm0 + q * 32);
+              bulk_commit();
+            }
+          } else if (rv && h < p.H) {
             __nv_bfloat16* arow = p.ob0 + j * 2 * p.H;
             uint4* a_dst = reinterpret_cast<uint4*>(arow + h);
             uint4* b_dst = reinterpret_cast<uint4*>(arow + p.H + h);
@@ -1223,13 +1269,37 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       } else if constexpr (MODE == kF2) {
         const bool rv = row_local < t.cvalid;
         const int64_t j = (int64_t)t.cm0 + row_local;
+        const bool whole = LRM_TC_FWD_STAGED && q * 32 + 32 <= t.cvalid;  // as in F1
 #pragma unroll 1
         for (int c = c_lo; c < c_hi; c += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + c, r);
           tmem_ld_wait();
           const int col = t.n0 + c;
-          if (rv && col < p.D) {
+          if (whole && col < p.D) {
+            uint4 yv[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(r[8 * v + u]);
+              yv[v] = Vec16<__nv_bfloat16>::pack(f);
+            }
+            // one y block per warp: a second one in turn measured slower
+            uint8_t* yb = wst;
+            if (lane == 0) bulk_wait_read(0);
+            __syncwarp();
+            const int sw = (lane >> 1) & 3;
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              *reinterpret_cast<uint4*>(yb + lane * 64 + ((v ^ sw) << 4)) = yv[v];
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&maps.o1, yb, col, t.cm0 + q * 32);
+              bulk_commit();
+            }
+          } else if (rv && col < p.D) {
             uint4* dst = reinterpret_cast<uint4*>(p.ob0 + j * p.D + col);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -1347,7 +1417,8 @@ static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs
 template <int MODE, bool PAIR>
 static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStream_t cs) {
   constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
-  p.stage_bufs = Geo<MODE>::kFwd ? 0
+  // forward: a, b and phi blocks (F1) or y blocks (F2) for the staged stores
+  p.stage_bufs = Geo<MODE>::kFwd ? (LRM_TC_FWD_STAGED ? (MODE == kF1 ? 2 : 1) : 0)
                  : Geo<MODE>::kWgrad                ? LRM_TC_WG_STAGE_BUFS
                                                     : LRM_TC_STAGE_BUFS;
   p.stages = MAX_STAGES;
@@ -1565,7 +1636,10 @@ lrm_status launch_fwd_tc(const FwdArgs& a, unsigned parts) {
         !make_map(&m.b, a.w_gate, false, 3, E, D, H, 64, 64) ||
         !make_map(&m.b2, a.w_up, false, 3, E, D, H, 64, 64))
       return LRM_ERR_CUDA;
-    m.o1 = m.o2 = m.b;
+    // ab and phi as 32 x 32 bf16 blocks (64-byte rows, 64-byte swizzle)
+    if (!make_map(&m.o1, a.ab, false, 2, 1, rows, 2 * H, 32, 32, 64)) return LRM_ERR_CUDA;
+    m.o2 = m.o1;
+    if (a.phi && !make_map(&m.o2, a.phi, false, 2, 1, rows, H, 32, 32, 64)) return LRM_ERR_CUDA;
     p.ob0 = reinterpret_cast<__nv_bfloat16*>(a.ab);
     p.ob1 = reinterpret_cast<__nv_bfloat16*>(a.phi);
     const int ntn = (H + BN / 2 - 1) / (BN / 2);
@@ -1577,7 +1651,9 @@ lrm_status launch_fwd_tc(const FwdArgs& a, unsigned parts) {
     if (!make_map(&m.a, a.phi, false, 2, 1, rows, H, 64, BM) ||
         !make_map(&m.b, a.w_down, false, 3, E, H, D, 64, 64))
       return LRM_ERR_CUDA;
-    m.b2 = m.o1 = m.o2 = m.b;
+    m.b2 = m.b;
+    if (!make_map(&m.o1, a.y, false, 2, 1, rows, D, 32, 32, 64)) return LRM_ERR_CUDA;
+    m.o2 = m.o1;
     p.ob0 = reinterpret_cast<__nv_bfloat16*>(a.y);
     p.ob1 = nullptr;
     const int ntn = (D + BN - 1) / BN;
