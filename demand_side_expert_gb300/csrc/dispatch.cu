@@ -4,10 +4,9 @@
 // Dispatch is a stable counting sort of the N = T*K pairs by expert id
 // ("Least-Loaded Expert Parallelism", Sec. 2.1 re-index and Alg. 4 sort of
 // the flattened indices; LRMoE Alg. 1 counts N_e). Up to 2^20 pairs it is one
-// launch of one 8-CTA cluster (dispatch_fused_kernel below); beyond that,
-// three launches with no inter-CTA waiting (with 128 experts the three
-// launches are faster from 2^17 pairs on, with 256 experts slower at 2^18,
-// measured on one GB300):
+// launch of one 16-CTA cluster (8 where the GPU cannot schedule 16;
+// dispatch_fused_kernel below); beyond that, three launches with no
+// inter-CTA waiting:
 //   1. per-chunk histogram (each CTA owns kChunk consecutive pairs),
 //   2. one CTA scans counts -> off and chunk bases (expert-major),
 //   3. each CTA replays its chunk warp by warp; inside a warp, lanes that
@@ -170,14 +169,16 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int n
 
 // ---------------------------------------------------------------------------
 // Single-launch variant for up to kFusedMaxPairs pairs: one cluster of
-// kFusedCtas CTAs. Each CTA counts its contiguous share of the pairs per warp
+// 16 CTAs (a non-portable cluster size, used where the GPU can schedule it),
+// else 8. Each CTA counts its contiguous share of the pairs per warp
 // (warp w of CTA c covers a contiguous sub-range, so warp order = pair order);
 // the CTAs read each other's per-expert counts through distributed shared
 // memory to get the expert offsets and their own bases, then replay their
 // share in order exactly like dispatch_scatter_kernel. No workspace, no
 // second launch, and the cluster barriers are hardware barriers (no spin).
 // ---------------------------------------------------------------------------
-constexpr int kFusedCtas = 8;
+constexpr int kFusedCtas = 8;         // portable cluster size
+constexpr int kFusedCtasMax = 16;     // non-portable cluster size, where available
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
 #ifndef LRM_DISPATCH_FUSED_MAX
@@ -201,7 +202,8 @@ __device__ __forceinline__ int ld_peer_smem(const int32_t* local, uint32_t rank)
   return v;
 }
 
-__global__ void __cluster_dims__(kFusedCtas, 1, 1) __launch_bounds__(kFusedThreads)
+// Launched as one cluster spanning the whole grid (gridDim.x CTAs).
+__global__ void __launch_bounds__(kFusedThreads)
 dispatch_fused_kernel(const int32_t* __restrict__ idx, int64_t N, int E,
                       int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                       int32_t* __restrict__ counts, int32_t* __restrict__ off, int32_t* err) {
@@ -214,7 +216,8 @@ dispatch_fused_kernel(const int32_t* __restrict__ idx, int64_t N, int E,
   __shared__ int total;
   const uint32_t rank = cluster_ctarank();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t per_cta = (N + kFusedCtas - 1) / kFusedCtas;
+  const int nctas = (int)gridDim.x;
+  const int64_t per_cta = (N + nctas - 1) / nctas;
   const int64_t per_warp = ((per_cta + kFusedWarps - 1) / kFusedWarps + 31) & ~int64_t(31);
   const int64_t c_lo = (int64_t)rank * per_cta, c_hi = min(N, c_lo + per_cta);
   const int64_t w_lo = min(c_hi, c_lo + w * per_warp), w_hi = min(c_hi, w_lo + per_warp);
@@ -243,7 +246,7 @@ dispatch_fused_kernel(const int32_t* __restrict__ idx, int64_t N, int E,
     const int e = e0 + threadIdx.x;
     int tot = 0, before = 0;
     if (e < E) {
-      for (uint32_t c = 0; c < kFusedCtas; ++c) {
+      for (uint32_t c = 0; c < (uint32_t)nctas; ++c) {
         const int v = ld_peer_smem(&cta_cnt[e], c);
         tot += v;
         if (c < rank) before += v;
@@ -371,8 +374,36 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
         cudaFuncSetAttribute(dispatch_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)shf) != cudaSuccess)
       return LRM_ERR_CUDA;
-    launch_k(dispatch_fused_kernel, dim3(kFusedCtas), dim3(kFusedThreads), shf, cs, 
-        topk_idx, N, E, perm, inv, counts, off, error_word(ws));
+    // 16 CTAs (twice the SMs) where a 16-CTA cluster of this kernel fits
+    // the GPU, else the portable 8
+    int nctas = kFusedCtas;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = shf;
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = LRM_PDL ? 2 : 1;
+    if (cudaFuncSetAttribute(dispatch_fused_kernel,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cfg.gridDim = dim3(kFusedCtasMax);
+      attr[0].val.clusterDim.x = kFusedCtasMax;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, dispatch_fused_kernel, &cfg) == cudaSuccess &&
+          clusters >= 1)
+        nctas = kFusedCtasMax;
+    }
+    (void)cudaGetLastError();  // a refused query leaves the portable size
+    cfg.gridDim = dim3(nctas);
+    attr[0].val.clusterDim.x = nctas;
+    if (cudaLaunchKernelEx(&cfg, dispatch_fused_kernel, topk_idx, N, E, perm, inv, counts, off,
+                           error_word(ws)) != cudaSuccess)
+      return LRM_ERR_CUDA;
     return launch_status();
   }
   const int nblk = dispatch_chunks(N);
