@@ -162,6 +162,15 @@ def roofline_of(a: dict, ms: float, peaks: dict) -> dict:
     return roof
 
 
+def roofline_time_ms(a: dict, peaks: dict) -> float:
+    """The least time a segment could take: its algorithmic bytes at the
+    measured copy bandwidth or its flops at the measured BF16 peak, whichever
+    is longer."""
+    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = a.get("flops", 0) / (peaks["bf16_tflops"] * 1e12)
+    return max(t_hbm, t_tc) * 1e3
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -454,6 +463,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         },
         "grouped_gemm_pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
         "grouped_gemm_tflops": round(gemm_tflops, 1),
+        # the four products' summed roofline times over their summed measured times
+        # (each product bound by HBM or the tensor pipe, whichever is slower)
+        "grouped_gemm_roofline_frac": round(
+            sum(roofline_time_ms(alg[s], peaks) for s in gemm) / gemm_ms, 4),
         "select_gbs": round(alg["select"]["bytes"] / (sel_ms * 1e-3) / 1e9, 1),
         "kernels": kernels,
         "roofline": roof,
