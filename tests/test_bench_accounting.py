@@ -1,0 +1,69 @@
+"""Host logic of bench.py's roofline accounting (no GPU).
+
+The roofline object divides algorithmic bytes or flops by a measured time;
+these tests pin the per-segment byte and flop counts to closed forms written
+out independently for the default layer, and check the bound selection and
+the summed-roofline fraction on hand-worked numbers.
+"""
+
+import pytest
+
+import bench
+from workloads import get_config
+
+PEAKS = {"hbm_gbs": 6792.4, "bf16_tflops": 1945.7}
+
+
+def test_expert_product_flops_are_twelve_dhm_in_total():
+    cfg = get_config("qwen3-30b-a3b-t4k")
+    M = 19707
+    a = bench.algorithmic(cfg, M, gathered=True)
+    D, H = cfg.D, cfg.H
+    # G1 and G2: D x H per retained row each; G3 and G4: D x 2H each (x2 flops per MAC)
+    assert a["fc2_dgrad"]["flops"] == a["fc2_wgrad"]["flops"] == 2 * M * D * H
+    assert a["fc1_wgrad"]["flops"] == a["fc1_dgrad"]["flops"] == 4 * M * D * H
+    assert sum(a[s]["flops"] for s in ("fc2_dgrad", "fc2_wgrad", "fc1_wgrad", "fc1_dgrad")) \
+        == 12 * D * H * M
+
+
+def test_weight_gradient_bytes_are_dominated_by_fp32_outputs():
+    cfg = get_config("qwen3-30b-a3b-t4k")
+    a = bench.algorithmic(cfg, 19707, gathered=True)
+    E, D, H = cfg.E, cfg.D, cfg.H
+    # dW_down (H x D) and dW_gate, dW_up (D x H each) in fp32, once per launch
+    assert a["fc2_wgrad"]["bytes"] >= 4 * E * H * D
+    assert a["fc1_wgrad"]["bytes"] >= 8 * E * D * H
+    # the default layer: 1.61 GB of fp32 FC1 weight gradients plus the rows
+    assert a["fc1_wgrad"]["bytes"] == 19707 * (D + 2 * H) * 2 + 8 * E * D * H
+
+
+def test_score_reads_every_g_and_phi_row_once():
+    cfg = get_config("qwen3-30b-a3b-t4k")
+    a = bench.algorithmic(cfg, 1, gathered=True)
+    N = cfg.T * cfg.K
+    assert a["score"]["bytes"] == cfg.T * cfg.D * 2 + N * cfg.H * 2 + 12 * N
+
+
+def test_gathered_compaction_moves_only_gradient_rows():
+    cfg = get_config("qwen3-30b-a3b-t4k")
+    M = 1000
+    g = bench.algorithmic(cfg, M, gathered=True)["compact"]["bytes"]
+    c = bench.algorithmic(cfg, M, gathered=False)["compact"]["bytes"]
+    assert c - g == 2 * M * (2 * cfg.D + 3 * cfg.H) * 2 - 2 * M * cfg.D * 2
+
+
+def test_roofline_picks_the_slower_bound():
+    # 1 GB and 100 GFLOP: HBM takes 147 us, the tensor pipe 51 us -> HBM-bound
+    r = bench.roofline_of({"bytes": 10 ** 9, "flops": 10 ** 11}, 0.2, PEAKS)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(5000.0, rel=1e-3)
+    assert r["frac"] == pytest.approx(5000.0 / 6792.4, rel=1e-3)
+    # 10 MB and 1 TFLOP: tensor-bound
+    r = bench.roofline_of({"bytes": 10 ** 7, "flops": 10 ** 12}, 1.0, PEAKS)
+    assert r["bound"] == "tensor" and r["achieved"] == pytest.approx(1000.0, rel=1e-3)
+
+
+def test_roofline_time_is_the_larger_of_the_two_bounds():
+    a = {"bytes": 6792.4e9 * 1e-3, "flops": 1945.7e12 * 2e-3}  # 1 ms of HBM, 2 ms of tensor
+    assert bench.roofline_time_ms(a, PEAKS) == pytest.approx(2.0)
+    assert bench.roofline_time_ms({"bytes": 6792.4e9 * 3e-3}, PEAKS) == pytest.approx(3.0)
