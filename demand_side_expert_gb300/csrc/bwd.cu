@@ -27,6 +27,7 @@ extern "C" lrm_status lrm_expert_fc2_dgrad(const lrm_shape* s, const int32_t* se
                                            const void* w_down, const void* dy_c,
                                            const void* ab_c, void* dab_c, void* ws,
                                            size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_fc2_dgrad");
   lrm_status st = check_common(s, ws, ws_bytes, sel_off);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {w_down}, {dy_c, ab_c, dab_c})) != LRM_OK) return st;
@@ -38,6 +39,7 @@ extern "C" lrm_status lrm_expert_fc2_dgrad(const lrm_shape* s, const int32_t* se
 extern "C" lrm_status lrm_expert_fc2_wgrad(const lrm_shape* s, const int32_t* sel_off,
                                            const void* phi_c, const void* dy_c, float* dw_down,
                                            void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_fc2_wgrad");
   lrm_status st = check_common(s, ws, ws_bytes, sel_off);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {dw_down}, {phi_c, dy_c})) != LRM_OK) return st;
@@ -50,6 +52,7 @@ extern "C" lrm_status lrm_expert_fc1_wgrad(const lrm_shape* s, const int32_t* se
                                            const void* x_c, const void* dab_c, float* dw_gate,
                                            float* dw_up, void* ws, size_t ws_bytes,
                                            void* stream) {
+  LRM_NVTX("lrm_expert_fc1_wgrad");
   lrm_status st = check_common(s, ws, ws_bytes, sel_off);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {dw_gate, dw_up}, {x_c, dab_c})) != LRM_OK) return st;
@@ -63,6 +66,7 @@ extern "C" lrm_status lrm_expert_fc1_dgrad(const lrm_shape* s, const int32_t* se
                                            const void* w_gate, const void* w_up,
                                            const void* dab_c, float* dx_c, void* ws,
                                            size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_fc1_dgrad");
   lrm_status st = check_common(s, ws, ws_bytes, sel_off);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {w_gate, w_up}, {dab_c, dx_c})) != LRM_OK) return st;
@@ -75,6 +79,7 @@ extern "C" lrm_status lrm_expert_fc1_dgrad(const lrm_shape* s, const int32_t* se
 extern "C" lrm_status lrm_scatter_dx(const lrm_shape* s, const float* dx_c, const int32_t* inv,
                                      const int32_t* row_of_pos, float* dx, void* ws,
                                      size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_scatter_dx");
   lrm_status st = check_shape(s);
   if (st != LRM_OK) return st;
   if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
@@ -88,6 +93,7 @@ extern "C" lrm_status lrm_expert_bwd_grouped(
     const void* w_down, const void* dy_c, const void* x_c, const void* ab_c, const void* phi_c,
     const int32_t* inv, const int32_t* row_of_pos, void* dab_c, float* dx_c, float* dw_gate,
     float* dw_up, float* dw_down, float* dx, void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_bwd_grouped");
   lrm_status st = check_common(s, ws, ws_bytes, sel_off);
   if (st != LRM_OK) return st;
   if (s->K > 32) return LRM_ERR_UNSUPPORTED;
@@ -101,6 +107,7 @@ extern "C" lrm_status lrm_expert_bwd_grouped(
 }
 
 extern "C" lrm_status lrm_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_selftest_wait_timeout");
   return selftest_wait_timeout(ws, ws_bytes, (cudaStream_t)stream);
 }
 
@@ -110,6 +117,7 @@ extern "C" lrm_status lrm_expert_bwd_gathered(
     const void* dy_c, const void* x, const void* ab, const void* phi, const int32_t* inv,
     const int32_t* row_of_pos, void* dab_c, float* dx_c, float* dw_gate, float* dw_up,
     float* dw_down, float* dx, void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_bwd_gathered");
   lrm_status st = check_common(s, ws, ws_bytes, sel_off);
   if (st != LRM_OK) return st;
   if (parts < 0 || parts > LRM_BWD_ALL) return LRM_ERR_INVALID_ARG;

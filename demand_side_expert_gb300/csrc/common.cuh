@@ -1,6 +1,7 @@
 // Shared host/device helpers of liblrm (validation, error word, vector I/O).
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -65,6 +66,17 @@ inline lrm_status check_ptrs(const lrm_shape* s, std::initializer_list<const voi
   }
   return LRM_OK;
 }
+
+// A named NVTX range around one C entry point, so timeline and profiler
+// tools (ncu --nvtx, a trace viewer) show which call launched which kernels;
+// with no tool attached it costs a check of a function pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define LRM_NVTX(name) ::lrm::NvtxRange lrm_nvtx_range_(name)
 
 inline lrm_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;

@@ -162,6 +162,7 @@ extern "C" lrm_status lrm_compact(const lrm_shape* s, const int32_t* perm,
                                   void* x_c, void* ab_c, void* phi_c, int32_t* tok_c,
                                   int32_t* row_of_pos, void* ws, size_t ws_bytes,
                                   void* stream) {
+  LRM_NVTX("lrm_compact");
   lrm_status st = check_shape(s);
   if (st != LRM_OK) return st;
   if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;

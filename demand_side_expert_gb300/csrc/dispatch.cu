@@ -341,6 +341,7 @@ extern "C" const char* lrm_status_string(lrm_status s) {
 }
 
 extern "C" lrm_status lrm_clear_device_error(void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_clear_device_error");
   if (!ws || ws_bytes < kWsHeaderBytes) return LRM_ERR_WORKSPACE;
   clear_header_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(error_word(ws));
   return launch_status();
@@ -348,6 +349,7 @@ extern "C" lrm_status lrm_clear_device_error(void* ws, size_t ws_bytes, void* st
 
 extern "C" lrm_status lrm_get_device_error(const void* ws, size_t ws_bytes,
                                            int32_t* code_out, void* stream) {
+  LRM_NVTX("lrm_get_device_error");
   if (!ws || ws_bytes < kWsHeaderBytes) return LRM_ERR_WORKSPACE;
   if (!code_out) return LRM_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LRM_ERR_CUDA;
@@ -360,6 +362,7 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
                                            int32_t* perm, int32_t* inv, int32_t* counts,
                                            int32_t* off, void* ws, size_t ws_bytes,
                                            void* stream) {
+  LRM_NVTX("lrm_dispatch_permute");
   lrm_status st = check_shape(s);
   if (st != LRM_OK) return st;
   if ((st = check_ws(s, ws, ws_bytes)) != LRM_OK) return st;
@@ -427,6 +430,7 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
 
 extern "C" lrm_status lrm_permute_rows(const int32_t* perm, int32_t n_rows, const void* src,
                                        void* dst, int64_t row_bytes, void* stream) {
+  LRM_NVTX("lrm_permute_rows");
   if (n_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return LRM_ERR_INVALID_ARG;
   if (n_rows == 0) return LRM_OK;
   if (!perm || !src || !dst) return LRM_ERR_INVALID_ARG;
@@ -442,6 +446,7 @@ extern "C" lrm_status lrm_permute_rows(const int32_t* perm, int32_t n_rows, cons
 extern "C" lrm_status lrm_quota_from_rate(const int32_t* counts, int32_t E, int32_t num,
                                           int32_t den, int32_t cap, int32_t* quota,
                                           void* stream) {
+  LRM_NVTX("lrm_quota_from_rate");
   if (E <= 0 || den <= 0 || num < 0 || num > den) return LRM_ERR_INVALID_ARG;
   if (!counts || !quota) return LRM_ERR_INVALID_ARG;
   launch_k(quota_kernel, dim3((E + 255) / 256), dim3(256), 0, (cudaStream_t)stream, counts, E, num, den, cap,

@@ -63,6 +63,7 @@ extern "C" lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* s, const int
                                                    int32_t* perm, int32_t* inv,
                                                    int32_t* counts, int32_t* off,
                                                    int32_t* dev_err, void* stream) {
+  LRM_NVTX("lrm_dispatch_permute_noalloc");
   lrm_status st = check_shape(s);
   if (st != LRM_OK) return st;
   const int64_t N = (int64_t)s->T * s->K;

@@ -132,6 +132,7 @@ using namespace lrm;
 
 extern "C" lrm_status lrm_gather_tokens(const lrm_shape* s, const int32_t* perm, const void* x,
                                         void* x_disp, void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_gather_tokens");
   lrm_status st = check_base(s, ws, ws_bytes);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {}, {perm, x, x_disp})) != LRM_OK) return st;
@@ -142,6 +143,7 @@ extern "C" lrm_status lrm_expert_fc1_fwd(const lrm_shape* s, const int32_t* off,
                                          const void* x_disp, const void* w_gate,
                                          const void* w_up, void* ab, void* phi, void* ws,
                                          size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_fc1_fwd");
   lrm_status st = check_base(s, ws, ws_bytes);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {off, w_gate, w_up}, {x_disp, ab, phi})) != LRM_OK) return st;
@@ -154,6 +156,7 @@ extern "C" lrm_status lrm_expert_fc1_fwd(const lrm_shape* s, const int32_t* off,
 extern "C" lrm_status lrm_expert_fc2_fwd(const lrm_shape* s, const int32_t* off,
                                          const void* phi, const void* w_down, void* y, void* ws,
                                          size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_fc2_fwd");
   lrm_status st = check_base(s, ws, ws_bytes);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {off, w_down}, {phi, y})) != LRM_OK) return st;
@@ -166,6 +169,7 @@ extern "C" lrm_status lrm_expert_fc2_fwd(const lrm_shape* s, const int32_t* off,
 extern "C" lrm_status lrm_combine(const lrm_shape* s, const void* y, const float* alpha,
                                   const int32_t* inv, float* out, void* ws, size_t ws_bytes,
                                   void* stream) {
+  LRM_NVTX("lrm_combine");
   lrm_status st = check_base(s, ws, ws_bytes);
   if (st != LRM_OK) return st;
   if (s->K > 32) return LRM_ERR_UNSUPPORTED;
@@ -180,6 +184,7 @@ extern "C" lrm_status lrm_expert_fwd_grouped(const lrm_shape* s, const int32_t* 
                                              const void* w_down, void* x_disp, void* ab,
                                              void* phi, void* y, float* out, void* ws,
                                              size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_fwd_grouped");
   lrm_status st = check_base(s, ws, ws_bytes);
   if (st != LRM_OK) return st;
   if (s->K > 32) return LRM_ERR_UNSUPPORTED;
@@ -198,6 +203,7 @@ extern "C" lrm_status lrm_expert_fc1_recompute(const lrm_shape* s, const int32_t
                                                const void* x_c, const void* w_gate,
                                                const void* w_up, void* ab_c, void* ws,
                                                size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_expert_fc1_recompute");
   lrm_status st = check_base(s, ws, ws_bytes);
   if (st != LRM_OK) return st;
   if ((st = check_ptrs(s, {sel_off, w_gate, w_up}, {x_c, ab_c})) != LRM_OK) return st;

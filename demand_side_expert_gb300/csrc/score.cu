@@ -189,6 +189,7 @@ static lrm_status score_entry(const lrm_shape* s, int metric, uint64_t seed, con
 extern "C" lrm_status lrm_score(const lrm_shape* s, const void* g, const void* phi,
                                 const float* alpha, const int32_t* inv, float* score,
                                 void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_score");
   return score_entry(s, LRM_METRIC_LRM, 0, g, phi, alpha, inv, score, ws, ws_bytes, stream);
 }
 
@@ -196,5 +197,6 @@ extern "C" lrm_status lrm_score_variant(const lrm_shape* s, int32_t metric, uint
                                         const void* g, const void* phi, const float* alpha,
                                         const int32_t* inv, float* score, void* ws,
                                         size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_score_variant");
   return score_entry(s, metric, seed, g, phi, alpha, inv, score, ws, ws_bytes, stream);
 }

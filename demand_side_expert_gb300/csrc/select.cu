@@ -343,6 +343,7 @@ extern "C" lrm_status lrm_select_quota(const lrm_shape* s, const float* score,
                                        const int32_t* off, const int32_t* quota,
                                        uint8_t* keep, int32_t* sel_off, int32_t* sel_pos,
                                        void* ws, size_t ws_bytes, void* stream) {
+  LRM_NVTX("lrm_select_quota");
   return select_entry<false>(s, score, off, const_cast<int32_t*>(quota), 0, 1, 0, keep,
                              sel_off, sel_pos, ws, ws_bytes, stream);
 }
@@ -352,6 +353,7 @@ extern "C" lrm_status lrm_select_rate(const lrm_shape* s, const float* score,
                                       int32_t* quota, uint8_t* keep, int32_t* sel_off,
                                       int32_t* sel_pos, void* ws, size_t ws_bytes,
                                       void* stream) {
+  LRM_NVTX("lrm_select_rate");
   return select_entry<true>(s, score, off, quota, num, den, cap, keep, sel_off, sel_pos, ws,
                             ws_bytes, stream);
 }
