@@ -638,3 +638,29 @@ def test_select_rate_equals_quota_then_select(dev):
         for k in ("quota", "sel_off"):
             assert torch.equal(getattr(a, k), getattr(b, k)), (rate, k)
         assert torch.equal(a.keep[:N], b.keep[:N]) and torch.equal(a.sel_pos[:M], b.sel_pos[:M])
+
+
+def test_selection_of_segments_beyond_the_shared_memory_key_stage(dev):
+    """The selection stages up to 40,960 keys of a segment in shared memory;
+    a larger segment is counted, copied to candidates and kept straight from
+    global memory. One expert here holds more than 40,960 pairs; three
+    criteria give it scores with many top bytes (LRM), few (squared gradient
+    norm) and uniform ones (random). Bit-exact against the oracle's selector
+    run on the GPU's scores, with the quotas the exact integer ceiling."""
+    cfg = get_config("qwen3-30b-a3b-t4k", T=65536, D=64, H=64, E=4, K=2)
+    inp = generate(cfg, device="cpu")
+    d = _to(inp, dev)
+    pipe = _pipe(cfg, dev)
+    pipe.dispatch(d["topk_idx"])
+    phi = pipe.to_dispatch_order(d["phi_pair"])
+    torch.cuda.synchronize()
+    perm, _, _, off = check_dispatch(pipe, inp["topk_idx"].numpy(), cfg.E)
+    assert np.diff(off).max() > 40960
+    for metric, rate in ((0, (1, 2)), (1, (3, 5)), (3, (1, 2)), (0, (1, 4))):
+        pipe.score_pairs(d["alpha"], d["g"], phi, metric=metric, seed=11)
+        pipe.select_rate(rate[0], rate[1], 0)
+        torch.cuda.synchronize()
+        assert pipe.device_error() == 0
+        quota = oracle.quota_from_rate(np.diff(off), rate[0], rate[1])
+        assert np.array_equal(to_np(pipe.quota), quota), (metric, rate)
+        check_selection(pipe, perm, off, quota)
