@@ -19,7 +19,10 @@ from test_gpu_parity import full_parity
 
 pytestmark = pytest.mark.gpu
 
-BF16_ROW_TOL = 2e-2  # relative L2 error per row: one BF16 rounding of each output
+# relative L2 error per row against the FP64 chain. A row of y or out has been
+# rounded twice on the way (phi, then y), each rounding at most 2^-9 relative
+# in BF16, so about 2e-3 per row: the same tolerance holds for every output.
+BF16_ROW_TOL = 2e-2
 F32_ROW_TOL = 1e-5
 
 
@@ -73,7 +76,7 @@ def forward_parity(cfg, dev, seed=None):
     check_rows(to_np(pipe.phi)[:N], f["phi"], tol, "phi")
     _, _, y_own = oracle.expert_fwd(f["off"], nin["w_gate"], nin["w_up"], nin["w_down"],
                                     f["x_disp"])
-    check_rows(to_np(pipe.y)[:N], y_own, 2 * tol, "y")
+    check_rows(to_np(pipe.y)[:N], y_own, tol, "y")
     y_from_gpu_phi = np.zeros_like(y_own)
     for e in range(cfg.E):
         lo, hi = int(f["off"][e]), int(f["off"][e + 1])
@@ -81,7 +84,7 @@ def forward_parity(cfg, dev, seed=None):
     check_rows(to_np(pipe.y)[:N], y_from_gpu_phi, tol, "y (GPU phi)")
     out_from_gpu_y = oracle.combine(to_np(pipe.y)[:N], nin["alpha"], f["inv"], cfg.K)
     check_rows(to_np(pipe.out)[:cfg.T], out_from_gpu_y, 1e-5, "out (GPU y)")
-    check_rows(to_np(pipe.out)[:cfg.T], f["out"], 2 * tol, "out")
+    check_rows(to_np(pipe.out)[:cfg.T], f["out"], tol, "out")
     return pipe, inp_cpu
 
 
@@ -179,7 +182,7 @@ def test_full_size_forward_qwen3_t4k(dev):
         idx = torch.as_tensor(sel, device=dev)
         check_rows(to_np(pipe.ab[idx]), ab, BF16_ROW_TOL, f"ab of expert {e}")
         check_rows(to_np(pipe.phi[idx]), phi, BF16_ROW_TOL, f"phi of expert {e}")
-        check_rows(to_np(pipe.y[idx]), y, 2 * BF16_ROW_TOL, f"y of expert {e}")
+        check_rows(to_np(pipe.y[idx]), y, BF16_ROW_TOL, f"y of expert {e}")
     # combine on sampled tokens from the GPU's own y rows
     y_all = pipe.y
     for t in rng.choice(cfg.T, size=64, replace=False):
