@@ -37,7 +37,14 @@ compact_kernel(const int32_t* __restrict__ perm, const uint8_t* __restrict__ kee
     if (!keep[i]) row_of_pos[i] = -1;
 
   const int lane = threadIdx.x & 31;
-  const int64_t M = sel_off[E];
+  // M = sel_off[E] comes from the caller's buffer: a value outside [0, N]
+  // (sel_off not written by the selection) is clamped and flagged, so no
+  // row past the N-row buffers is ever addressed
+  int64_t M = sel_off[E];
+  if (M < 0 || M > N) {
+    if (gtid == 0) flag_error(err, LRM_DEVERR_INDEX);
+    M = M < 0 ? 0 : N;
+  }
   const int dv = D / V, abv = 2 * H / V, hv = H / V;
   {  // 64 zero rows of dy_c after the retained ones: the padding the FC2
      // weight-gradient product reads as B past the last group

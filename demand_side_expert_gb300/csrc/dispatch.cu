@@ -375,8 +375,10 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
     const size_t shf = ((size_t)kFusedWarps * E + 2 * E) * 4;
     if (shf > 48 * 1024 &&
         cudaFuncSetAttribute(dispatch_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)shf) != cudaSuccess)
+                             (int)shf) != cudaSuccess) {
+      (void)cudaGetLastError();  // leave no error behind for a later call to report
       return LRM_ERR_CUDA;
+    }
     // 16 CTAs (twice the SMs) where a 16-CTA cluster of this kernel fits
     // the GPU, else the portable 8
     int nctas = kFusedCtas;

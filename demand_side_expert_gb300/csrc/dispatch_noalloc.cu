@@ -85,8 +85,10 @@ extern "C" lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* s, const int
                              (int)sh1) != cudaSuccess ||
         cudaFuncSetAttribute(dispatch_scatter_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sh3) != cudaSuccess)
+                             (int)sh3) != cudaSuccess) {
+      (void)cudaGetLastError();  // leave no error behind for a later call to report
       return LRM_ERR_CUDA;
+    }
   }
   dispatch_hist_kernel<<<(int)nblk, kDispThreads, sh1, cs>>>(topk_idx, N, E, (int)nblk,
                                                              chunk_hist, dev_err);

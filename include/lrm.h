@@ -209,6 +209,10 @@ lrm_status lrm_select_quota(const lrm_shape* shape, const float* score,
  * may be NULL too (see lrm_expert_fc1_recompute, which rebuilds [a | b], and
  * lrm_expert_bwd_gathered, which reads x, ab and phi rows in place). A
  * non-NULL destination with a NULL source is an error.
+ * M is read from sel_off[E] on the device: a value outside [0, N] (sel_off
+ * not produced by a selection call) is clamped into that range and flags
+ * LRM_DEVERR_INDEX in the workspace error word; out-of-range sel_pos or perm
+ * entries are skipped and flag the same bit.
  */
 lrm_status lrm_compact(const lrm_shape* shape, const int32_t* perm,
                        const uint8_t* keep, const int32_t* sel_off,

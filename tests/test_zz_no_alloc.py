@@ -57,6 +57,53 @@ def test_noalloc_dispatch_matches_workspace_dispatch_twice(name, over):
             assert torch.equal(a[:n], b[:n])
 
 
+def test_noalloc_dispatch_with_1024_experts():
+    """1024 experts: the count and scatter kernels need more than 48 KiB of
+    shared memory, so the call first raises their limit; the result is the
+    workspace dispatch's (its single-cluster kernel) bit for bit, twice."""
+    from demand_side_expert_gb300 import lrm
+
+    dev = torch.device("cuda:0")
+    cfg = get_config("qwen3-30b-a3b-t4k", T=1024, D=64, H=64, E=1024, K=8)
+    N, E = cfg.N, cfg.E
+    shape = lrm.make_shape(cfg.T, cfg.D, cfg.H, cfg.E, cfg.K, lrm.LRM_BF16)
+    idx = generate(cfg, device=dev)["topk_idx"]
+    ref = _reference(lrm, shape, idx, N, E, dev)
+    for _ in range(2):
+        got = _buffers(N, E, dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        lrm.lrm_dispatch_permute_noalloc(shape, idx, *got, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        for a, b, n in zip(ref, got, (N, N, E, E + 1)):
+            assert torch.equal(a[:n], b[:n])
+
+
+def test_noalloc_dispatch_allocates_no_device_memory():
+    """After a first call (which may load the kernels and look up the
+    scratch array's address), further calls leave the device's free memory
+    and PyTorch's allocator untouched."""
+    from demand_side_expert_gb300 import lrm
+
+    dev = torch.device("cuda:0")
+    cfg = get_config("stress-e256", D=64, H=64)
+    N, E = cfg.N, cfg.E
+    shape = lrm.make_shape(cfg.T, cfg.D, cfg.H, cfg.E, cfg.K, lrm.LRM_BF16)
+    idx = generate(cfg, device=dev)["topk_idx"]
+    got = _buffers(N, E, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lrm.lrm_dispatch_permute_noalloc(shape, idx, *got, err)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    alloc0 = torch.cuda.memory_allocated(dev)
+    for _ in range(3):
+        lrm.lrm_dispatch_permute_noalloc(shape, idx, *got, err)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info(dev)[0] == free0
+    assert torch.cuda.memory_allocated(dev) == alloc0
+    assert int(err.item()) == 0
+
+
 def test_noalloc_flags_bad_ids_like_the_workspace_path():
     from demand_side_expert_gb300 import lrm
 
