@@ -5,11 +5,14 @@
 // the squared Frobenius norm of the rank-one contribution (alpha_u g_t) phi_u^T
 // to the protected FC2 weight gradient, computed without forming it.
 //
-// One warp per token: the loads of the token's cotangent row g_t and of its
-// K saved FC2-input rows phi_u (found through inv, up to 8 at a time) are all
-// issued before any reduction, so some thirty 16-byte loads per lane are in
-// flight. HBM-bound: every byte of g and phi is read exactly once with
-// 128-bit streaming loads.
+// One warp per token. HBM-bound: every byte of g and phi is read exactly once
+// with 128-bit streaming loads. The time is set by how many bytes each SM
+// keeps in flight: for BF16 layers with up to 8 routed experts per token the
+// kernel is instantiated with compile-time counts of 16-byte chunks per lane
+// (GV for the cotangent row g_t, HV for each saved FC2-input row phi_u), so
+// every load of the token is issued before any reduction (one memory round
+// trip per token); other shapes take a generic kernel that sweeps the rows
+// with runtime bounds.
 #include <algorithm>
 
 #include "common.cuh"
@@ -36,6 +39,18 @@ __device__ __forceinline__ float row_sq_partial(const T* row, int n_vec, int lan
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < V; ++i) s += acc[i];
+  return s;
+}
+
+// Sum of squares of one 16-byte vector of activations.
+template <typename T>
+__device__ __forceinline__ float sum_sq(const uint4& v) {
+  constexpr int V = Vec16<T>::kElems;
+  float f[V];
+  Vec16<T>::unpack(v, f);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) s = fmaf(f[i], f[i], s);
   return s;
 }
 
@@ -132,6 +147,88 @@ score_kernel(const T* __restrict__ g, const T* __restrict__ phi,
   }
 }
 
+// LRM score with every load of the token issued up front: GV 16-byte chunks
+// of g_t and HV of each of the token's (at most 8) phi rows per lane,
+// predicated on the actual row lengths (D / 8 and H / 8 chunks).
+constexpr int kUpfrontThreads = 128;
+
+template <int GV, int HV>
+__global__ void __launch_bounds__(kUpfrontThreads)
+score_upfront_kernel(const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* __restrict__ phi,
+                     const float* __restrict__ alpha, const int32_t* __restrict__ inv,
+                     float* __restrict__ score, int ntok, int D, int H, int K, int32_t* err) {
+  pdl_begin();  // predecessor complete before any global access
+  const int lane = threadIdx.x & 31;
+  const int64_t N = (int64_t)ntok * K;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int gv = D / 8, hv = H / 8;
+  for (int64_t t = warp; t < ntok; t += nwarps) {
+    // lane k: dispatch position of slot k; a bad entry is flagged, its row
+    // read at position 0 and its score not written
+    int my_pos = 0, my_dst = -1;
+    if (lane < K) {
+      const int q = inv[t * K + lane];
+      if (q >= 0 && q < N) my_pos = my_dst = q;
+      else flag_error(err, LRM_DEVERR_INDEX);
+    }
+    const uint4* grow = reinterpret_cast<const uint4*>(g + t * D);
+    uint4 vg[GV], vp[kRowsInFlight][HV];
+#pragma unroll
+    for (int i = 0; i < GV; ++i) {
+      const int c = lane + 32 * i;
+      vg[i] = c < gv ? ld_stream(grow + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsInFlight; ++r) {
+      const int pos = __shfl_sync(0xffffffffu, my_pos, r);
+      const uint4* prow = reinterpret_cast<const uint4*>(phi + (int64_t)pos * H);
+#pragma unroll
+      for (int i = 0; i < HV; ++i) {
+        const int c = lane + 32 * i;
+        vp[r][i] = (r < K && c < hv) ? ld_stream(prow + c) : make_uint4(0, 0, 0, 0);
+      }
+    }
+    float gpart = 0.f;
+#pragma unroll
+    for (int i = 0; i < GV; ++i) gpart += sum_sq<__nv_bfloat16>(vg[i]);
+    const float gsq = warp_sum(gpart);
+#pragma unroll
+    for (int r = 0; r < kRowsInFlight; ++r) {
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < HV; ++i) part += sum_sq<__nv_bfloat16>(vp[r][i]);
+      const float psq = warp_sum(part);
+      const int dst = __shfl_sync(0xffffffffu, my_dst, r);
+      if (lane == 0 && dst >= 0) {
+        const float a = alpha[t * K + r];
+        score[dst] = (a * a) * gsq * psq;
+      }
+    }
+  }
+}
+
+// The smallest instantiation that covers the layer (chunks per lane), or
+// nullptr when none does (then the generic kernel runs).
+using UpfrontKernel = void (*)(const __nv_bfloat16*, const __nv_bfloat16*, const float*,
+                               const int32_t*, float*, int, int, int, int, int32_t*);
+
+static UpfrontKernel pick_upfront(int D, int H, int K) {
+  if (K > kRowsInFlight) return nullptr;
+  const int gl = (D / 8 + 31) / 32, hl = (H / 8 + 31) / 32;
+#define LRM_UPFRONT(GVv, HVv) \
+  if (gl <= GVv && hl <= HVv) return score_upfront_kernel<GVv, HVv>;
+  if (gl <= 8) {
+    LRM_UPFRONT(8, 1) LRM_UPFRONT(8, 2) LRM_UPFRONT(8, 3) LRM_UPFRONT(8, 4) LRM_UPFRONT(8, 6)
+  }
+  if (gl <= 16) {
+    LRM_UPFRONT(16, 1) LRM_UPFRONT(16, 2) LRM_UPFRONT(16, 3) LRM_UPFRONT(16, 4)
+    LRM_UPFRONT(16, 6)
+  }
+#undef LRM_UPFRONT
+  return nullptr;
+}
+
 template <typename T>
 static void launch_score(const lrm_shape* s, int metric, uint64_t seed, const void* g,
                          const void* phi, const float* alpha, const int32_t* inv, float* score,
@@ -175,9 +272,21 @@ static lrm_status score_entry(const lrm_shape* s, int metric, uint64_t seed, con
     return LRM_ERR_INVALID_ARG;
   if ((needs_g && !aligned16(g)) || (needs_phi && !aligned16(phi))) return LRM_ERR_UNSUPPORTED;
   const int64_t warps = s->T;
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (s->dtype == LRM_BF16 && metric == LRM_METRIC_LRM) {
+    if (UpfrontKernel kern = pick_upfront(s->D, s->H, s->K)) {
+      // a warp per token, all of them at once where the grid allows
+      const int64_t per_cta = kUpfrontThreads / 32;
+      const int64_t cap = (int64_t)num_sms() * 64;
+      const int blocks = (int)std::min((warps + per_cta - 1) / per_cta, cap);
+      launch_k(kern, dim3(blocks), dim3(kUpfrontThreads), 0, cs, (const __nv_bfloat16*)g,
+               (const __nv_bfloat16*)phi, alpha, inv, score, s->T, s->D, s->H, s->K,
+               error_word(ws));
+      return launch_status();
+    }
+  }
   const int64_t cap = (int64_t)num_sms() * (2048 / kScoreThreads) * (kScoreThreads / 32);
   const int blocks = (int)((std::min(warps, cap) + 7) / 8);
-  cudaStream_t cs = (cudaStream_t)stream;
   if (s->dtype == LRM_BF16)
     launch_score<__nv_bfloat16>(s, metric, seed, g, phi, alpha, inv, score, error_word(ws),
                                 blocks, cs);

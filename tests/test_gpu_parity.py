@@ -119,6 +119,16 @@ def test_explicit_quotas_and_extremes(dev):
     full_parity(cfg, dev, (1, 1), quota=quota.astype(np.int32))
 
 
+@pytest.mark.parametrize("over", [
+    dict(T=256, D=128, H=1664, E=8, K=4),   # phi rows longer than the up-front kernels hold
+    dict(T=128, D=128, H=128, E=16, K=10),  # more than 8 routed experts per token
+])
+def test_bf16_score_generic_kernel(dev, over):
+    """BF16 shapes outside the up-front score kernel's instantiations take the
+    generic kernel; the whole path still matches the oracle."""
+    full_parity(get_config("qwen3-30b-a3b-t4k", **over), dev, (1, 2))
+
+
 @pytest.mark.parametrize("over,rate", [
     (dict(T=300, D=128, H=64, E=6, K=1), (1, 2)),   # top-1 routing
     (dict(T=200, D=128, H=64, E=1, K=1), (3, 5)),   # one expert holding every token
