@@ -9,6 +9,13 @@ retained rows per second, M / step time, with M = sum_e q_e the retained
 token-expert pairs. The L2 is flushed (a 256 MiB write) before every timed
 step, outside the step's CUDA events.
 
+The default layer is the largest single-GPU workload, shaped like
+GLM4.5-106B-A12B (T = 16384, D = 4096, H = 1408, E = 128, top-8, BF16); the
+headline is its rho = 1/2 point, and the same line carries the whole
+retention sweep (rho = 1/4, 1/2, 3/4, 1 at fixed routed pairs N) with a
+least-squares fit of step time against the retained rows M, plus one timed
+pass of each other workload (``configs``).
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
@@ -33,7 +40,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "retained-pair expert-backward rows/s; grouped-GEMM % BF16 peak; select GB/s"
-DEFAULT_CONFIG = "qwen3-30b-a3b-t4k"
+DEFAULT_CONFIG = "glm45-106b-a12b-t16k"
+# the other workloads timed once each into the line's "configs" table
+OTHER_WORKLOADS = ["qwen3-30b-a3b-t4k", "qwen3-30b-a3b-t32k", "stress-e256"]
 FLUSH_BYTES = 256 << 20
 SEGMENTS = ["dispatch", "score", "select", "compact", "fc2_dgrad", "fc2_wgrad",
             "fc1_wgrad", "fc1_dgrad", "scatter_dx"]
@@ -101,6 +110,10 @@ def parse_args():
                     help="supplementary: time the dispatch permutation and the selection "
                          "(with the quota rule) alone over routed-pair counts 2^15..2^22 "
                          "and print one JSON line; the headline run is not made")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the retention sweep of a workload that has several rates")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads into the line's configs table")
     ap.add_argument("--no-recompute", action="store_true",
                     help="skip the timing of the backward step that recomputes [a | b]")
     return ap.parse_args()
@@ -288,34 +301,23 @@ def workload_of(args):
     return cfg
 
 
-def run_ours(args, rank: int, world: int, local_rank: int):
-    import torch
+def headline_rate(cfg, args):
+    """The retention rate of the headline line: --rate, else the middle of a
+    retention sweep (rho = 1/2 on the GLM-shaped layer), else the workload's rate."""
+    if args.rate:
+        return tuple(int(v) for v in args.rate.split("/"))
+    if (1, 2) in cfg.rates:
+        return (1, 2)
+    return cfg.rates[0]
 
-    from demand_side_expert_gb300 import RecalibratedExpertBackward, lrm
-    from workloads import generate
 
-    gathered = args.backward == "gathered"
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-    cfg = workload_of(args)
-    rate = tuple(int(v) for v in args.rate.split("/")) if args.rate else cfg.rates[0]
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    inp = generate(cfg, device=dev, seed=cfg.seed + rank)
-    pipe = RecalibratedExpertBackward(cfg.T, cfg.D, cfg.H, cfg.E, cfg.K, cfg.dtype, dev)
-    # forward side, once: dispatch and the saved state in dispatch order
-    pipe.dispatch(inp["topk_idx"])
-    ab = pipe.to_dispatch_order(inp["ab_pair"])
-    phi = pipe.to_dispatch_order(inp["phi_pair"])
-    del inp["ab_pair"], inp["phi_pair"]
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
+def make_step(pipe, inp, ab, phi, rate, cfg, stream, gathered):
+    """One step of the whole path as a function of a list of events: with
+    seg=False only its first and last events are recorded, so consecutive
+    kernels overlap as they do without timing."""
+    from demand_side_expert_gb300 import lrm
 
     def step(ev, seg=True):
-        """One step; with seg=False only its first and last events are
-        recorded, so consecutive kernels overlap as they do without timing."""
         def mark(j):
             if seg or j == 0 or j == len(SEGMENTS):
                 ev[j].record(stream)
@@ -348,51 +350,214 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         pipe.scatter_dx()
         mark(9)
 
+    return step
+
+
+def time_layer(pipe, inp, ab, phi, rate, cfg, flush, stream, steps, warmup, gathered,
+               dist=None):
+    """Warm-up, then `steps` headline steps (events at their two ends only,
+    the L2 flushed before each, outside the events), then a second pass of
+    `steps` steps with an event between every call for the per-segment
+    times. Returns the retained rows and the times in ms."""
+    import torch
+
+    step = make_step(pipe, inp, ab, phi, rate, cfg, stream, gathered)
+    dev = pipe.device
+
     def new_events():
         return [torch.cuda.Event(enable_timing=True) for _ in range(len(SEGMENTS) + 1)]
 
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    for _ in range(max(args.warmup, 0)):
+    for _ in range(max(warmup, 0)):
         flush.fill_(1)
         step(new_events())
     torch.cuda.synchronize(dev)
     if pipe.device_error() != 0:
         raise RuntimeError(f"device error word {pipe.device_error()} after warm-up")
     M = pipe.retained_rows
-
-    events = [new_events() for _ in range(args.steps)]
+    events = [new_events() for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         flush.fill_(1)  # L2 flush outside the step's events
         step(events[i], seg=False)
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     wall = time.perf_counter() - wall0
-    # per-segment times from a second pass with an event between every call
-    # (the events keep consecutive kernels from overlapping; not the headline)
-    seg_events = [new_events() for _ in range(args.steps)]
-    for i in range(args.steps):
+    seg_events = [new_events() for _ in range(steps)]
+    for i in range(steps):
         flush.fill_(1)
         step(seg_events[i], seg=True)
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-
-    seg_ms = {s: [] for s in SEGMENTS}
-    for ev in seg_events:
-        for j, s in enumerate(SEGMENTS):
-            seg_ms[s].append(ev[j].elapsed_time(ev[j + 1]))
-    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
-    seg_step_ms = statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in seg_events)
-    total_s = sum(step_ms) / 1e3
     if pipe.device_error() != 0:
         raise RuntimeError(f"device error word {pipe.device_error()} after timing")
+    seg_ms = {s: [ev[j].elapsed_time(ev[j + 1]) for ev in seg_events]
+              for j, s in enumerate(SEGMENTS)}
+    return {"M": M, "step_ms": [ev[0].elapsed_time(ev[-1]) for ev in events],
+            "seg_ms": seg_ms,
+            "seg_step_ms": statistics.mean(ev[0].elapsed_time(ev[-1]) for ev in seg_events),
+            "wall": wall}
 
+
+def largest_segment(pipe) -> int:
+    return int(pipe.counts.max().item()) if pipe.E else 0
+
+
+def layer_summary(cfg, rate, t: dict, peaks: dict, gathered: bool, n_max: int) -> dict:
+    """Per-kernel times, GB/s and TFLOP/s, the dominant kernel's roofline and
+    the grouped products' totals of one timed layer."""
+    M = t["M"]
+    seg_ms = t["seg_ms"]
+    alg = algorithmic(cfg, M, gathered)
+    traffic = load_traffic(cfg.name)
+    kernels = {}
+    for s in SEGMENTS:
+        ms = statistics.mean(seg_ms[s])
+        k = {"ms": round(ms, 4), "kernels": segment_kernels(s, cfg.N),
+             "gbs": round(alg[s]["bytes"] / (ms * 1e-3) / 1e9, 1),
+             "frac_hbm": round(alg[s]["bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        if "flops" in alg[s]:
+            k["tflops"] = round(alg[s]["flops"] / (ms * 1e-3) / 1e12, 1)
+            k["frac_bf16"] = round(alg[s]["flops"] / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                   4)
+        if s in traffic:  # DRAM bytes of one launch from an ncu capture of this build
+            k["dram_bytes"] = traffic[s]
+            k["dram_gbs"] = round(traffic[s] / (ms * 1e-3) / 1e9, 1)
+        kernels[s] = k
+    # the selection is one CTA per expert: its time is set by the largest
+    # segment, not by bytes (latency-bound)
+    kernels["select"]["us"] = round(1e3 * kernels["select"]["ms"], 2)
+    kernels["select"]["bound"] = "latency (one CTA per expert; the largest segment sets it)"
+    kernels["select"]["largest_segment"] = n_max
+    if "dram_bytes" not in kernels["compact"]:
+        kernels["compact"]["dram_bytes"] = None
+    kernels["compact"]["note"] = (
+        "gbs counts the algorithmic bytes (a token's g row once per retained pair); "
+        "dram_gbs counts the DRAM bytes ncu measured for one launch (g rows re-read from L2)")
+    dominant = max(SEGMENTS, key=lambda s: statistics.mean(seg_ms[s]))
+    a = alg[dominant]
+    roof = roofline_of(a, statistics.mean(seg_ms[dominant]), peaks)
+    roof["traffic"] = traffic.get(dominant)
+    roof["kernel"] = KERNEL_NAMES[dominant]
+    roof["algorithmic_bytes"] = a["bytes"]
+    if "flops" in a:
+        roof["algorithmic_flops"] = a["flops"]
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst)" \
+        if peaks["source"] == "measured" else "fallback"
+    gemm = ["fc2_dgrad", "fc2_wgrad", "fc1_wgrad", "fc1_dgrad"]
+    gemm_ms = sum(statistics.mean(seg_ms[s]) for s in gemm)
+    gemm_flops = sum(alg[s]["flops"] for s in gemm)
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    ms = statistics.mean(t["step_ms"])
+    return {
+        "rho": f"{rate[0]}/{rate[1]}", "retained_rows": M, "ms_per_step": round(ms, 4),
+        "rows_per_s": round(M / (ms * 1e-3), 1),
+        "ms_per_step_with_segment_events": round(t["seg_step_ms"], 4),
+        "grouped_gemm_tflops": round(gemm_tflops, 1),
+        "grouped_gemm_pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
+        # the four products' summed roofline times over their summed measured times
+        # (each product bound by HBM or the tensor pipe, whichever is slower)
+        "grouped_gemm_roofline_frac": round(
+            sum(roofline_time_ms(alg[s], peaks) for s in gemm) / gemm_ms, 4),
+        "select_gbs": round(alg["select"]["bytes"] / (kernels["select"]["ms"] * 1e-3) / 1e9, 1),
+        "kernels": kernels, "roofline": roof,
+    }
+
+
+def linear_fit(xs, ys) -> dict:
+    """Least-squares line y = a + b x with R^2 and the largest residual."""
+    n = len(xs)
+    mx, my = sum(xs) / n, sum(ys) / n
+    sxx = sum((x - mx) ** 2 for x in xs)
+    b = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sxx if sxx else 0.0
+    a = my - b * mx
+    res = [y - (a + b * x) for x, y in zip(xs, ys)]
+    sst = sum((y - my) ** 2 for y in ys)
+    r2 = 1.0 - sum(r * r for r in res) / sst if sst else 1.0
+    return {"a": a, "b": b, "r2": r2, "max_abs_residual": max(abs(r) for r in res)}
+
+
+def sweep_summary(cfg, points: list, peaks: dict) -> dict:
+    """Step time against retained rows M over a retention sweep at fixed N."""
+    fit = linear_fit([p["retained_rows"] for p in points], [p["ms_per_step"] for p in points])
+    s = 2 if cfg.dtype == "bf16" else 4
+    fixed_bytes = 3 * cfg.E * cfg.D * cfg.H * (s + 4)  # weights in, FP32 weight gradients out
+    return {
+        "routed_pairs": cfg.N,
+        "points": points,
+        "fit": {"model": "ms_per_step = intercept_ms + ns_per_retained_row * M / 1e6",
+                "intercept_ms": round(fit["a"], 4),
+                "ns_per_retained_row": round(fit["b"] * 1e6, 3),
+                "r2": round(fit["r2"], 5),
+                "max_abs_residual_us": round(fit["max_abs_residual"] * 1e3, 1)},
+        "intercept_reading": {
+            "weights_in_and_fp32_weight_gradients_out_bytes": fixed_bytes,
+            "their_time_at_measured_hbm_ms": round(fixed_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3,
+                                                   4)},
+    }
+
+
+def prepare_layer(cfg, dev, seed):
+    """Generate one layer, allocate its buffers and lay out the saved state in
+    dispatch order (the forward side, done once, not timed)."""
+    from demand_side_expert_gb300 import RecalibratedExpertBackward
+    from workloads import generate
+
+    inp = generate(cfg, device=dev, seed=seed)
+    pipe = RecalibratedExpertBackward(cfg.T, cfg.D, cfg.H, cfg.E, cfg.K, cfg.dtype, dev)
+    pipe.dispatch(inp["topk_idx"])
+    ab = pipe.to_dispatch_order(inp["ab_pair"])
+    phi = pipe.to_dispatch_order(inp["phi_pair"])
+    del inp["ab_pair"], inp["phi_pair"]
+    return inp, pipe, ab, phi
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    from workloads import get_config
+
+    gathered = args.backward == "gathered"
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    cfg = workload_of(args)
+    rate = headline_rate(cfg, args)
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp, pipe, ab, phi = prepare_layer(cfg, dev, cfg.seed + rank)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t = time_layer(pipe, inp, ab, phi, rate, cfg, flush, stream, args.steps, args.warmup,
+                   gathered, dist)
+    n_max = largest_segment(pipe)
+    M = t["M"]
+    total_s = sum(t["step_ms"]) / 1e3
     total_max, rows_sum = aggregate_ranks(total_s, M * args.steps, dev, dist)
+    peaks = load_peaks()
+
+    # the retention sweep of a layer that has one: same N, growing M
+    sweep = None
+    if len(cfg.rates) > 1 and not args.no_sweep and not args.rate:
+        points = []
+        for r in cfg.rates:
+            tr = t if r == rate else time_layer(pipe, inp, ab, phi, r, cfg, flush, stream,
+                                                args.steps, args.warmup, gathered)
+            sm = layer_summary(cfg, r, tr, peaks, gathered, n_max)
+            points.append({k: sm[k] for k in (
+                "rho", "retained_rows", "ms_per_step", "rows_per_s",
+                "grouped_gemm_tflops", "grouped_gemm_pct_bf16_peak",
+                "grouped_gemm_roofline_frac", "select_gbs")}
+                | {"segments_ms": {s: sm["kernels"][s]["ms"] for s in SEGMENTS},
+                   "score_frac_hbm": sm["kernels"]["score"]["frac_hbm"],
+                   "compact_frac_hbm": sm["kernels"]["compact"]["frac_hbm"]})
+        sweep = sweep_summary(cfg, points, peaks)
 
     e2e = None
     if not args.no_e2e:
@@ -407,38 +572,34 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if not args.no_other_backward:
         other = run_other_backward(pipe, inp, ab, phi, rate, cfg, flush, stream, args)
 
+    # the other workloads, one pass each with the same timing and L2 flush
+    others = None
+    if not args.no_configs and not args.override:
+        del pipe, inp, ab, phi
+        torch.cuda.empty_cache()
+        others = {}
+        for name in OTHER_WORKLOADS:
+            if name == cfg.name:
+                continue
+            ocfg = get_config(name)
+            orate = ocfg.rates[0]
+            oinp, opipe, oab, ophi = prepare_layer(ocfg, dev, ocfg.seed + rank)
+            ot = time_layer(opipe, oinp, oab, ophi, orate, ocfg, flush, stream, args.steps,
+                            args.warmup, gathered)
+            sm = layer_summary(ocfg, orate, ot, peaks, gathered, largest_segment(opipe))
+            sm["workload"] = ocfg.name
+            sm["T"], sm["D"], sm["H"], sm["E"], sm["K"] = ocfg.T, ocfg.D, ocfg.H, ocfg.E, ocfg.K
+            sm["quota_cap"] = ocfg.cap
+            sm["gpu_launches"] = kernels_per_step(ocfg.N) * 2 * args.steps
+            others[name] = sm
+            del oinp, opipe, oab, ophi
+            torch.cuda.empty_cache()
+    clk = clocks.stop()
+
     if rank != 0:
         return None
 
-    peaks = load_peaks()
-    alg = algorithmic(cfg, M, gathered)
-    traffic = load_traffic(cfg.name)
-    kernels = {}
-    for s in SEGMENTS:
-        ms = statistics.mean(seg_ms[s])
-        k = {"ms": round(ms, 4), "kernels": segment_kernels(s, cfg.N),
-             "gbs": round(alg[s]["bytes"] / (ms * 1e-3) / 1e9, 1)}
-        if "flops" in alg[s]:
-            k["tflops"] = round(alg[s]["flops"] / (ms * 1e-3) / 1e12, 1)
-        kernels[s] = k
-    dominant = max(SEGMENTS, key=lambda s: statistics.mean(seg_ms[s]))
-    dom_ms = statistics.mean(seg_ms[dominant])
-    a = alg[dominant]
-    roof = roofline_of(a, dom_ms, peaks)
-    roof["traffic"] = traffic.get(dominant)
-    roof["kernel"] = KERNEL_NAMES[dominant]
-    roof["algorithmic_bytes"] = a["bytes"]
-    if "flops" in a:
-        roof["algorithmic_flops"] = a["flops"]
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json burst)" \
-        if peaks["source"] == "measured" else "fallback"
-
-    gemm = ["fc2_dgrad", "fc2_wgrad", "fc1_wgrad", "fc1_dgrad"]
-    gemm_ms = sum(statistics.mean(seg_ms[s]) for s in gemm)
-    gemm_flops = sum(alg[s]["flops"] for s in gemm)
-    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
-    sel_ms = statistics.mean(seg_ms["select"])
-
+    head = layer_summary(cfg, rate, t, peaks, gathered, n_max)
     line = {
         "metric": METRIC,
         "value": round(rows_sum / total_max, 1),
@@ -447,33 +608,34 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(total_max * 1e3 / args.steps, 4),
-        "ms_per_step_with_segment_events": round(seg_step_ms, 4),
+        "ms_per_step_with_segment_events": head["ms_per_step_with_segment_events"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic (seeded router, SwiGLU forward state and cotangents)",
         "config": {
-            "workload": cfg.name, "T": cfg.T, "D": cfg.D, "H": cfg.H, "E": cfg.E, "K": cfg.K,
+            "workload": f"{cfg.name} rho={rate[0]}/{rate[1]}", "layer": cfg.name,
+            "T": cfg.T, "D": cfg.D, "H": cfg.H, "E": cfg.E, "K": cfg.K,
             "rho": f"{rate[0]}/{rate[1]}", "quota_cap": cfg.cap, "routed_pairs": cfg.N,
             "retained_rows": M, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
             "inputs": "resident in HBM",
             "backward": args.backward,
         },
-        "grouped_gemm_pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
-        "grouped_gemm_tflops": round(gemm_tflops, 1),
-        # the four products' summed roofline times over their summed measured times
-        # (each product bound by HBM or the tensor pipe, whichever is slower)
-        "grouped_gemm_roofline_frac": round(
-            sum(roofline_time_ms(alg[s], peaks) for s in gemm) / gemm_ms, 4),
-        "select_gbs": round(alg["select"]["bytes"] / (sel_ms * 1e-3) / 1e9, 1),
-        "kernels": kernels,
-        "roofline": roof,
-        "gpu_launches": kernels_per_step(cfg.N) * args.steps,
+        "grouped_gemm_pct_bf16_peak": head["grouped_gemm_pct_bf16_peak"],
+        "grouped_gemm_tflops": head["grouped_gemm_tflops"],
+        "grouped_gemm_roofline_frac": head["grouped_gemm_roofline_frac"],
+        "select_gbs": head["select_gbs"],
+        "kernels": head["kernels"],
+        "roofline": head["roofline"],
+        # headline steps and the segmented pass over them
+        "gpu_launches": kernels_per_step(cfg.N) * 2 * args.steps,
         "clocks": clk,
-        "wall_s": round(wall, 4),
+        "wall_s": round(t["wall"], 4),
     }
+    if sweep is not None:
+        line["rho_sweep"] = sweep
     if e2e is not None:
         line["e2e"] = e2e
     if fwd is not None:
@@ -482,6 +644,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line["recompute"] = rec
     if other is not None:
         line["other_backward"] = other
+    if others:
+        line["configs"] = others
     return line, cfg, rate
 
 
@@ -754,9 +918,11 @@ def cpu_baseline(cfg, rate, T_s: int):
 
 def oracle_tokens(cfg, rate, seconds: float) -> int:
     """Tokens whose oracle pass takes about ``seconds`` on the host: a fixed
-    ~1 s (weight-gradient buffers) plus 12*D*H float64 flops per retained row
-    at ~32 GFLOP/s."""
-    rows = max(seconds - 1.0, 0.5) * 3.2e10 / (12.0 * cfg.D * cfg.H)
+    part (first touch of the float64 weight-gradient buffers, 3*E*D*H*8
+    bytes, at about 8 GB/s) plus 12*D*H float64 flops per retained row at
+    about 90 GFLOP/s (NumPy's BLAS on 16 Arm cores)."""
+    fixed = 3.0 * cfg.E * cfg.D * cfg.H * 8 / 8e9
+    rows = max(seconds - fixed, 0.5) * 9e10 / (12.0 * cfg.D * cfg.H)
     tokens = int(rows / (cfg.K * rate[0] / rate[1] if rate[0] else cfg.K))
     return max(16, min(cfg.T, tokens))
 
@@ -765,7 +931,7 @@ def run_reference(args, rank: int):
     if rank != 0:
         return None
     cfg = workload_of(args)
-    rate = tuple(int(v) for v in args.rate.split("/")) if args.rate else cfg.rates[0]
+    rate = headline_rate(cfg, args)
     per_step = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
     small, a = oracle_sample(cfg, rate, oracle_tokens(cfg, rate, per_step), cfg.seed)
     for _ in range(max(args.warmup, 0)):

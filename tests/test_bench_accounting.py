@@ -67,3 +67,37 @@ def test_roofline_time_is_the_larger_of_the_two_bounds():
     a = {"bytes": 6792.4e9 * 1e-3, "flops": 1945.7e12 * 2e-3}  # 1 ms of HBM, 2 ms of tensor
     assert bench.roofline_time_ms(a, PEAKS) == pytest.approx(2.0)
     assert bench.roofline_time_ms({"bytes": 6792.4e9 * 3e-3}, PEAKS) == pytest.approx(3.0)
+
+
+def test_linear_fit_recovers_a_line_and_its_residuals():
+    xs = [32818, 65569, 98353, 131072]
+    ys = [1.87 + 4.972e-5 * x for x in xs]
+    f = bench.linear_fit(xs, ys)
+    assert f["a"] == pytest.approx(1.87, rel=1e-9)
+    assert f["b"] == pytest.approx(4.972e-5, rel=1e-9)
+    assert f["r2"] == pytest.approx(1.0)
+    ys2 = [1.0, 3.0, 2.0, 4.0]  # hand-worked: slope 0.8, intercept 0.5, residuals +-0.3/0.6
+    g = bench.linear_fit([1, 2, 3, 4], ys2)
+    assert g["b"] == pytest.approx(0.8) and g["a"] == pytest.approx(0.5)
+    assert g["max_abs_residual"] == pytest.approx(0.9)
+    assert g["r2"] == pytest.approx(1 - 1.8 / 5.0)
+
+
+def test_sweep_reports_the_fit_in_ns_per_row_and_the_fixed_bytes():
+    cfg = get_config("glm45-106b-a12b-t16k")
+    pts = [{"retained_rows": m, "ms_per_step": 2.0 + 5e-5 * m} for m in (1000, 2000, 4000)]
+    s = bench.sweep_summary(cfg, pts, PEAKS)
+    assert s["fit"]["ns_per_retained_row"] == pytest.approx(50.0)
+    assert s["fit"]["intercept_ms"] == pytest.approx(2.0)
+    fixed = s["intercept_reading"]["weights_in_and_fp32_weight_gradients_out_bytes"]
+    assert fixed == 3 * 128 * 4096 * 1408 * 6  # BF16 weights in, FP32 gradients out
+    assert s["routed_pairs"] == cfg.N
+
+
+def test_headline_rate_is_the_middle_of_a_sweep():
+    class A:
+        rate = None
+    assert bench.headline_rate(get_config("glm45-106b-a12b-t16k"), A()) == (1, 2)
+    assert bench.headline_rate(get_config("qwen3-30b-a3b-t4k"), A()) == (3, 5)
+    A.rate = "3/4"
+    assert bench.headline_rate(get_config("glm45-106b-a12b-t16k"), A()) == (3, 4)
