@@ -557,7 +557,6 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr bool WG = Geo<MODE>::kWgrad;
   constexpr int BNL = Cfg<PAIR>::kBRows;
   constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
-  constexpr int NBOX = (BM + BNL) / 64;  // 64x64 MN-major boxes per stage (wgrad)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -857,13 +856,13 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
               load3(b_s + i * BOX_BYTES, mapB, nb0 + 64 * i, kb * BK, t.e);
           } else {
             const int y = t.row0 + kb * BK;
-            if (!gathered_a) {
-#pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                load2(a_s + i * BOX_BYTES, mapA, t.cm0 + 64 * i, y);
-            }
-#pragma unroll
-            for (int i = 0; i < BNL / 64; ++i) load2(b_s + i * BOX_BYTES, mapB, nb0 + 64 * i, y);
+            // one copy per operand: the maps view a row as 64-column chunks
+            // (x: column in the chunk, y: row, z: chunk), so a box of 64 rows
+            // by several chunks lands as consecutive 64 x 64 blocks. (One copy
+            // per 64 x 64 box made the even CTA of a pair re-issue each ring
+            // slot about 1.6 us late.)
+            if (!gathered_a) load3(a_s, mapA, 0, y, t.cm0 / 64);
+            load3(b_s, mapB, 0, y, nb0 / 64);
           }
           if (to_leader) {
             mbar_arrive_cluster_relaxed(bar_cl);
@@ -1397,6 +1396,24 @@ static bool make_map(CUtensorMap* m, const void* base, bool fp32, int rank, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major [rows, cols] bf16 matrix (cols a multiple of 64) seen as 3-D
+// {64 columns, rows, cols / 64 chunks}: a box of 64 rows by `chunks` chunks
+// lands in shared memory as `chunks` consecutive 64 x 64 blocks (128-byte
+// swizzle), the layout of that many separate 64 x 64 boxes.
+static bool make_chunked_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                             uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || cols % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, 64, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
 
 static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs) {
@@ -1478,10 +1495,11 @@ static lrm_status launch_any(const Maps& single, const Maps& pair, const Params&
 // Weight-gradient products with gathered A rows run on single CTAs (the
 // gather producer is written for one CTA per tile).
 template <int MODE>
-static lrm_status launch_gather_or_any(const Maps& m, const Params& p, int64_t tiles_single,
-                                       int64_t tiles_pair, cudaStream_t cs) {
+static lrm_status launch_gather_or_any(const Maps& m, const Maps& mp, const Params& p,
+                                       int64_t tiles_single, int64_t tiles_pair,
+                                       cudaStream_t cs) {
   if (p.a_rows) return launch_mode<MODE, false>(m, p, tiles_single, cs);
-  return launch_any<MODE>(m, m, p, tiles_single, tiles_pair, cs);
+  return launch_any<MODE>(m, mp, p, tiles_single, tiles_pair, cs);
 }
 
 }  // namespace tc
@@ -1530,8 +1548,8 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
   };
   // K-major operands (data-gradient products): 64 x 128 A boxes and 64 x 256
   // (single CTA) or 64 x 128 (pair) weight boxes, one expert per 3-D slice;
-  // MN-major operands (weight-gradient products): 64 x 64 boxes; fp32
-  // outputs: 32 x 32 boxes.
+  // MN-major operands (weight-gradient products): 64 rows by 2 or 4 chunks of
+  // 64 columns per copy; fp32 outputs: 32 x 32 boxes.
   if (parts & kPartFc2Dgrad) {
     Maps m1, m2;
     if (!make_map(&m1.a, a.dy_c, false, 2, 1, rows, D, 64, BM) ||
@@ -1552,39 +1570,48 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     p.ab_rows = nullptr;
   }
   if (parts & kPartFc2Wgrad) {
-    Maps m;
-    if (!make_map(&m.a, a.phi_c, false, 2, 1, rows, H, 64, 64) ||
-        !make_map(&m.b, a.dy_c, false, 2, 1, rows, D, 64, 64) ||
-        !make_map(&m.o1, a.dw_down, true, 3, E, H, D, 32, 32))
+    Maps m, mp;  // single CTAs (B: 256 columns) and CTA pairs (B: 128 per CTA)
+    if (!make_map(&m.o1, a.dw_down, true, 3, E, H, D, 32, 32) ||
+        !make_chunked_map(&m.a, a.phi_c, rows, H, BM / 64) ||
+        !make_chunked_map(&m.b, a.dy_c, rows, D, BN / 64) ||
+        !make_chunked_map(&mp.b, a.dy_c, rows, D, BN / 128))
       return LRM_ERR_CUDA;
     m.b2 = m.b;
     m.o2 = m.o1;
+    mp.a = m.a;
+    mp.b2 = mp.b;
+    mp.o1 = mp.o2 = m.o1;
     p.out0 = a.dw_down;
     p.a_rows = gathered ? a.sel_pos : nullptr;
     p.a_src = reinterpret_cast<const __nv_bfloat16*>(a.phi_c);
     p.a_src_rows = (int)N;
     p.a_src_cols = H;
-    if ((st = launch_gather_or_any<kG2>(m, p, wg_tiles(BM, H, D), wg_tiles(2 * BM, H, D),
+    if ((st = launch_gather_or_any<kG2>(m, mp, p, wg_tiles(BM, H, D), wg_tiles(2 * BM, H, D),
                                         a.stream)) != LRM_OK)
       return st;
     p.a_rows = nullptr;
   }
   if (parts & kPartFc1Wgrad) {
-    Maps m;
-    if (!make_map(&m.a, a.x_c, false, 2, 1, gathered ? tok_rows : rows, D, 64, 64) ||
-        !make_map(&m.b, a.dab_c, false, 2, 1, rows, 2 * H, 64, 64) ||
-        !make_map(&m.o1, a.dw_gate, true, 3, E, D, H, 32, 32) ||
-        !make_map(&m.o2, a.dw_up, true, 3, E, D, H, 32, 32))
+    Maps m, mp;  // single CTAs (B: 256 columns) and CTA pairs (B: 128 per CTA)
+    if (!make_map(&m.o1, a.dw_gate, true, 3, E, D, H, 32, 32) ||
+        !make_map(&m.o2, a.dw_up, true, 3, E, D, H, 32, 32) ||
+        !make_chunked_map(&m.a, a.x_c, gathered ? tok_rows : rows, D, BM / 64) ||
+        !make_chunked_map(&m.b, a.dab_c, rows, 2 * H, BN / 64) ||
+        !make_chunked_map(&mp.b, a.dab_c, rows, 2 * H, BN / 128))
       return LRM_ERR_CUDA;
     m.b2 = m.b;
+    mp.a = m.a;
+    mp.b2 = mp.b;
+    mp.o1 = m.o1;
+    mp.o2 = m.o2;
     p.out0 = a.dw_gate;
     p.out1 = a.dw_up;
     p.a_rows = gathered ? a.tok_c : nullptr;
     p.a_src = reinterpret_cast<const __nv_bfloat16*>(a.x_c);
     p.a_src_rows = s->T;
     p.a_src_cols = D;
-    if ((st = launch_gather_or_any<kG3>(m, p, wg_tiles(BM, D, 2 * H), wg_tiles(2 * BM, D, 2 * H),
-                                        a.stream)) != LRM_OK)
+    if ((st = launch_gather_or_any<kG3>(m, mp, p, wg_tiles(BM, D, 2 * H),
+                                        wg_tiles(2 * BM, D, 2 * H), a.stream)) != LRM_OK)
       return st;
     p.a_rows = nullptr;
   }
