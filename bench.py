@@ -4,7 +4,7 @@
 One step = one pass of the whole path over one synthetic MoE layer with its
 inputs resident in HBM: dispatch permutation, LRM score, quota rule and
 per-expert top-q selection, compaction, the four grouped expert-backward
-products and the dx scatter (9 kernel launches up to 2^20 routed pairs). The metric is
+products and the dx scatter (9 kernel launches up to 2^17 routed pairs). The metric is
 retained rows per second, M / step time, with M = sum_e q_e the retained
 token-expert pairs. The L2 is flushed (a 256 MiB write) before every timed
 step, outside the step's CUDA events.
@@ -54,7 +54,7 @@ KERNEL_NAMES = {
     "fc1_wgrad": "grouped_gemm_kernel<2, 0>", "fc1_dgrad": "grouped_gemm_kernel<3, 1>",
     "scatter_dx": "dx_gather_kernel",
 }
-FUSED_DISPATCH_MAX_PAIRS = 1 << 20  # above it dispatch takes three launches
+FUSED_DISPATCH_MAX_PAIRS = 1 << 17  # above it dispatch takes three launches
 # the forward expert pass that produces the saved state, timed on its own
 FWD_SEGMENTS = ["dispatch", "gather", "fc1_fwd", "fc2_fwd", "combine"]
 FWD_KERNEL_NAMES = {
@@ -919,10 +919,10 @@ def cpu_baseline(cfg, rate, T_s: int):
 def oracle_tokens(cfg, rate, seconds: float) -> int:
     """Tokens whose oracle pass takes about ``seconds`` on the host: a fixed
     part (first touch of the float64 weight-gradient buffers, 3*E*D*H*8
-    bytes, at about 8 GB/s) plus 12*D*H float64 flops per retained row at
-    about 90 GFLOP/s (NumPy's BLAS on 16 Arm cores)."""
-    fixed = 3.0 * cfg.E * cfg.D * cfg.H * 8 / 8e9
-    rows = max(seconds - fixed, 0.5) * 9e10 / (12.0 * cfg.D * cfg.H)
+    bytes, at about 16 GB/s) plus 12*D*H float64 flops per retained row at
+    about 250 GFLOP/s (NumPy's BLAS on 16 Arm cores, as measured)."""
+    fixed = 3.0 * cfg.E * cfg.D * cfg.H * 8 / 1.6e10
+    rows = max(seconds - fixed, 0.5) * 2.5e11 / (12.0 * cfg.D * cfg.H)
     tokens = int(rows / (cfg.K * rate[0] / rate[1] if rate[0] else cfg.K))
     return max(16, min(cfg.T, tokens))
 
@@ -959,10 +959,11 @@ def run_reference(args, rank: int):
 
 
 def run_index_sweep(args):
-    """The two latency-bound index steps at growing N = T*K (K = 8, E = 128, zipf-skewed
+    """The latency-bound index steps at growing N = T*K (K = 8, E = 128, zipf-skewed
     routing, rho = 1/2, random scores), each timed alone with CUDA events (L2 flushed
-    before every launch). GB/s counts the algorithmic bytes: dispatch 4N + 16N + 8E,
-    selection 4N + N + 4M + 16E."""
+    before every launch): dispatch, selection with the quota rule, and the standalone
+    quota rule. GB/s counts the algorithmic bytes: dispatch 4N + 16N + 8E, selection
+    4N + N + 4M + 16E."""
     import torch
     from demand_side_expert_gb300 import lrm
 
@@ -992,6 +993,8 @@ def run_index_sweep(args):
                                                          ws, ws_bytes, None),
             "select": lambda: lrm.lrm_select_rate(shape, score, off, num, den, 0, quota, keep,
                                                   sel_off, sel_pos, ws, ws_bytes, None),
+            # the standalone quota rule (the step folds it into the selection)
+            "quota": lambda: lrm.lrm_quota_from_rate(counts, E, num, den, 0, quota, None),
         }
         point = {"N": N}
         for name, fn in calls.items():

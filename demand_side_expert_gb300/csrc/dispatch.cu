@@ -3,14 +3,16 @@
 //
 // Dispatch is a stable counting sort of the N = T*K pairs by expert id
 // ("Least-Loaded Expert Parallelism", Sec. 2.1 re-index and Alg. 4 sort of
-// the flattened indices; LRMoE Alg. 1 counts N_e). Up to 2^20 pairs it is one
+// the flattened indices; LRMoE Alg. 1 counts N_e). Up to 2^17 pairs it is one
 // launch of one 16-CTA cluster (8 where the GPU cannot schedule 16;
 // dispatch_fused_kernel below); beyond that, three launches with no
 // inter-CTA waiting:
 //   1. per-chunk histogram (each CTA owns kChunk consecutive pairs),
-//   2. one CTA scans counts -> off and chunk bases (expert-major),
-//   3. each CTA replays its chunk warp by warp; inside a warp, lanes that
-//      share an expert are ranked with __match_any_sync, so positions follow
+//   2. one CTA per expert scans that expert's chunk counts: the chunk's first
+//      position inside the expert's segment, and the expert's count,
+//   3. each CTA derives the expert offsets from the counts (a block scan),
+//      then replays its chunk warp by warp; inside a warp, lanes that share
+//      an expert are ranked with __match_any_sync, so positions follow
 //      ascending pair index (stability) without atomics on the output.
 #include <algorithm>
 
@@ -104,41 +106,58 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
   return r;
 }
 
+// One CTA per expert e: chunk_rel[e][b] = sum of the expert's counts in chunks
+// before b (its first position inside the expert's segment); counts[e] = the
+// expert's total. Chunks are scanned a block-width at a time with a carry.
 __global__ void __launch_bounds__(1024)
 dispatch_scan_kernel(const int32_t* __restrict__ chunk_hist, int E, int nblk,
-                     int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
-                     int32_t* __restrict__ off) {
+                     int32_t* __restrict__ chunk_rel, int32_t* __restrict__ counts) {
   pdl_begin();  // predecessor complete before any global access
   __shared__ int warp_tot[32];
   __shared__ int total;
-  const int e = threadIdx.x;
-  int n = 0;
-  if (e < E)
-    for (int b = 0; b < nblk; ++b) n += chunk_hist[(int64_t)e * nblk + b];
-  const int excl = block_exclusive_scan(e < E ? n : 0, warp_tot, &total);
-  if (e < E) {
-    counts[e] = n;
-    off[e] = excl;
-    int run = excl;
-    for (int b = 0; b < nblk; ++b) {
-      chunk_base[(int64_t)e * nblk + b] = run;
-      run += chunk_hist[(int64_t)e * nblk + b];
-    }
+  const int e = blockIdx.x;
+  if (e >= E) return;
+  const int32_t* h = chunk_hist + (int64_t)e * nblk;
+  int32_t* rel = chunk_rel + (int64_t)e * nblk;
+  int carry = 0;
+  for (int b0 = 0; b0 < nblk; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    const int v = b < nblk ? h[b] : 0;
+    const int excl = block_exclusive_scan(v, warp_tot, &total);
+    if (b < nblk) rel[b] = carry + excl;
+    carry += total;  // read before any thread can pass the next scan's first barrier
   }
-  if (threadIdx.x == 0) off[E] = total;
+  if (threadIdx.x == 0) counts[e] = carry;
 }
 
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, int64_t N, int E, int nblk,
-                        const int32_t* __restrict__ chunk_base,
+                        const int32_t* __restrict__ chunk_rel,
+                        const int32_t* __restrict__ counts, int32_t* __restrict__ off,
                         int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
   pdl_begin();  // predecessor complete before any global access
   extern __shared__ int32_t sh[];
   int32_t* hist = sh;                       // [8][E]
   int32_t* run = sh + kDispWarps * E;       // [8][E] next position per warp
-  chunk_histogram(idx, N, E, hist, nullptr);
+  int32_t* eoff = run + kDispWarps * E;     // [E] expert offsets
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  // expert offsets: exclusive scan of the counts, a block-width at a time
+  int carry = 0;
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    const int v = e < E ? counts[e] : 0;
+    const int excl = block_exclusive_scan(v, warp_tot, &total);
+    if (e < E) {
+      eoff[e] = carry + excl;
+      if (blockIdx.x == 0) off[e] = carry + excl;
+    }
+    carry += total;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) off[E] = carry;
+  chunk_histogram(idx, N, E, hist, nullptr);  // starts with a barrier: eoff is visible
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int acc = chunk_base[(int64_t)e * nblk + blockIdx.x];
+    int acc = eoff[e] + chunk_rel[(int64_t)e * nblk + blockIdx.x];
     for (int w = 0; w < kDispWarps; ++w) {
       run[w * E + e] = acc;
       acc += hist[w * E + e];
@@ -182,7 +201,7 @@ constexpr int kFusedCtasMax = 16;     // non-portable cluster size, where availa
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
 #ifndef LRM_DISPATCH_FUSED_MAX
-#define LRM_DISPATCH_FUSED_MAX (1 << 20)
+#define LRM_DISPATCH_FUSED_MAX (1 << 17)
 #endif
 constexpr int64_t kFusedMaxPairs = LRM_DISPATCH_FUSED_MAX;
 
@@ -413,9 +432,9 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
   }
   const int nblk = dispatch_chunks(N);
   int32_t* chunk_hist = reinterpret_cast<int32_t*>((char*)ws + kWsHeaderBytes);
-  int32_t* chunk_base = chunk_hist + (int64_t)E * nblk;
+  int32_t* chunk_rel = chunk_hist + (int64_t)E * nblk;
   const size_t sh1 = (size_t)kDispWarps * E * 4;
-  const size_t sh3 = 2 * sh1;
+  const size_t sh3 = 2 * sh1 + (size_t)E * 4;
   if (sh3 > 48 * 1024) {
     cudaFuncSetAttribute(dispatch_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sh1);
@@ -424,9 +443,10 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
   }
   launch_k(dispatch_hist_kernel, dim3(nblk), dim3(kDispThreads), sh1, cs, topk_idx, N, E, nblk, chunk_hist,
                                                         error_word(ws));
-  launch_k(dispatch_scan_kernel, dim3(1), dim3(1024), 0, cs, chunk_hist, E, nblk, chunk_base, counts, off);
+  launch_k(dispatch_scan_kernel, dim3(E), dim3(1024), 0, cs, chunk_hist, E, nblk, chunk_rel,
+           counts);
   launch_k(dispatch_scatter_kernel, dim3(nblk), dim3(kDispThreads), sh3, cs, topk_idx, N, E, nblk,
-                                                           chunk_base, perm, inv);
+           (const int32_t*)chunk_rel, (const int32_t*)counts, off, perm, inv);
   return launch_status();
 }
 

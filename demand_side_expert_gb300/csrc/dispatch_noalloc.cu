@@ -23,10 +23,10 @@ namespace lrm {
 __global__ void dispatch_hist_kernel(const int32_t* idx, int64_t N, int E, int nblk,
                                      int32_t* chunk_hist, int32_t* err);
 __global__ void dispatch_scan_kernel(const int32_t* chunk_hist, int E, int nblk,
-                                     int32_t* chunk_base, int32_t* counts, int32_t* off);
+                                     int32_t* chunk_rel, int32_t* counts);
 __global__ void dispatch_scatter_kernel(const int32_t* idx, int64_t N, int E, int nblk,
-                                        const int32_t* chunk_base, int32_t* perm,
-                                        int32_t* inv);
+                                        const int32_t* chunk_rel, const int32_t* counts,
+                                        int32_t* off, int32_t* perm, int32_t* inv);
 
 namespace {
 
@@ -34,7 +34,8 @@ constexpr int kChunkPairs = 2048;   // pairs per CTA, as in dispatch.cu
 constexpr int kDispThreads = 256;
 constexpr int kDispWarps = kDispThreads / 32;
 
-// Count table [E][chunks] followed by base table [E][chunks].
+// Count table [E][chunks] followed by the table of each chunk's first position
+// inside its expert's segment [E][chunks].
 static __device__ __align__(256) int32_t g_dispatch_scratch[2 * LRM_NOALLOC_MAX_CHUNK_ENTRIES];
 
 // Device address of g_dispatch_scratch, resolved once per device.
@@ -76,10 +77,10 @@ extern "C" lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* s, const int
   // Both tables are written in full before they are read, so the previous
   // call's contents need no clearing.
   int32_t* chunk_hist = scratch;
-  int32_t* chunk_base = scratch + (int64_t)E * nblk;
+  int32_t* chunk_rel = scratch + (int64_t)E * nblk;
   cudaStream_t cs = (cudaStream_t)stream;
   const size_t sh1 = (size_t)kDispWarps * E * 4;
-  const size_t sh3 = 2 * sh1;
+  const size_t sh3 = 2 * sh1 + (size_t)E * 4;
   if (sh3 > 48 * 1024) {
     if (cudaFuncSetAttribute(dispatch_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sh1) != cudaSuccess ||
@@ -92,8 +93,9 @@ extern "C" lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* s, const int
   }
   dispatch_hist_kernel<<<(int)nblk, kDispThreads, sh1, cs>>>(topk_idx, N, E, (int)nblk,
                                                              chunk_hist, dev_err);
-  dispatch_scan_kernel<<<1, 1024, 0, cs>>>(chunk_hist, E, (int)nblk, chunk_base, counts, off);
+  dispatch_scan_kernel<<<E, 1024, 0, cs>>>(chunk_hist, E, (int)nblk, chunk_rel, counts);
   dispatch_scatter_kernel<<<(int)nblk, kDispThreads, sh3, cs>>>(topk_idx, N, E, (int)nblk,
-                                                                chunk_base, perm, inv);
+                                                                chunk_rel, counts, off, perm,
+                                                                inv);
   return launch_status();
 }

@@ -221,10 +221,10 @@ def test_deterministic_repeats(dev):
                 assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("T", [131072, 131073])
+@pytest.mark.parametrize("T", [16384, 16385, 131073])
 def test_dispatch_either_side_of_the_single_launch_limit(dev, T):
-    """2^20 routed pairs take the one-cluster launch, 2^20 + 8 the three launches;
-    both are the oracle's stable counting sort, bit for bit."""
+    """2^17 routed pairs take the one-cluster launch, 2^17 + 8 and 2^20 + 8 the three launches;
+    all are the oracle's stable counting sort, bit for bit."""
     cfg = get_config("qwen3-30b-a3b-t4k", T=T, D=64, H=64)
     inp = generate(cfg, device="cpu")
     pipe = _pipe(cfg, dev)
