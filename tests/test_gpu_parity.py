@@ -300,7 +300,7 @@ def _oracle_rows(perm, sel_pos, lo, hi, alpha, x, g, ab, phi, K):
 
 
 def _full_size(name, rate, cap=0, sample_experts=5, sample_tokens=64, seed=None,
-               gathered=True, chunk=8192):
+               gathered=True, chunk=8192, every=False):
     """A full-size layer in the launch configuration bench.py times (by
     default the gathered backward). The oracle builds every operand from the
     layer's inputs itself: its own dispatch-order layout of the saved state,
@@ -314,7 +314,10 @@ def _full_size(name, rate, cap=0, sample_experts=5, sample_tokens=64, seed=None,
     within one rounding of alpha*g (and, with the compacted backward, every
     copied row of x_c, ab_c and phi_c bit for bit); weight gradients and the
     data-gradient rows of sampled experts and dx of sampled tokens within
-    2e-2 relative Frobenius error."""
+    2e-2 relative Frobenius error. With ``every``, the weight gradients and
+    data-gradient rows of every expert (exact zeros for experts with no
+    retained row) and dx of every token, the latter summed by the oracle's
+    own scatter from its own rows."""
     cfg = get_config(name)
     dev = torch.device("cuda:0")
     inp = generate(cfg, device=dev, seed=seed)
@@ -354,9 +357,13 @@ def _full_size(name, rate, cap=0, sample_experts=5, sample_tokens=64, seed=None,
     rng = np.random.default_rng(0)
     m = np.diff(sel_off)
     nonempty = np.nonzero(m)[0]
-    picks = {int(np.argmax(m)), int(nonempty[np.argmin(m[nonempty])])}
-    picks |= set(int(e) for e in rng.choice(nonempty, size=min(sample_experts, nonempty.size),
-                                            replace=False))
+    if every:
+        picks = set(range(cfg.E))
+        dxc_all = np.zeros((M, cfg.D))
+    else:
+        picks = {int(np.argmax(m)), int(nonempty[np.argmin(m[nonempty])])}
+        picks |= set(int(e) for e in rng.choice(nonempty, size=min(sample_experts, nonempty.size),
+                                                replace=False))
     wcache = {}
 
     def weights(e):
@@ -366,6 +373,10 @@ def _full_size(name, rate, cap=0, sample_experts=5, sample_tokens=64, seed=None,
 
     for e in sorted(picks):
         lo, hi = int(sel_off[e]), int(sel_off[e + 1])
+        if hi == lo:  # no retained row: the weight gradients are exactly zero
+            for k in ("dw_gate", "dw_up", "dw_down"):
+                assert not getattr(pipe, k)[e].any(), (name, e, k)
+            continue
         c = _oracle_rows(perm, sel_pos, lo, hi, alpha, x, g, ab, phi, K)
         b = oracle.expert_bwd(np.array([0, hi - lo]), *weights(e), c["dy_c"], c["x_c"],
                               c["ab_c"], c["phi_c"])
@@ -375,6 +386,16 @@ def _full_size(name, rate, cap=0, sample_experts=5, sample_tokens=64, seed=None,
         for k in ("dab_c", "dx_c"):
             err = rel_fro(to_np(getattr(pipe, k)[lo:hi]), b[k])
             assert err <= 2e-2, (name, e, k, err)
+        if every:
+            dxc_all[lo:hi] = b["dx_c"]
+    if every:  # dx of every token from the oracle's rows and its own scatter
+        want = oracle.dx_gather(dxc_all, inv, rop, cfg.T, K)
+        got = _f64(pipe.dx[:cfg.T])
+        err = np.linalg.norm(got - want, axis=1)
+        lim = 2e-2 * np.maximum(np.linalg.norm(want, axis=1), 1e-12)
+        assert (err <= lim).all(), (name, "dx", int((err > lim).sum()))
+        assert rel_fro(got, want) <= 2e-2
+        return pipe
     # dx on sampled tokens: the oracle's rows of the token's kept slots, summed
     for t in rng.choice(cfg.T, size=min(sample_tokens, cfg.T), replace=False):
         want = np.zeros(cfg.D)
@@ -393,22 +414,24 @@ def _full_size(name, rate, cap=0, sample_experts=5, sample_tokens=64, seed=None,
 
 
 def test_full_size_qwen3_t4k(dev):
-    _full_size("qwen3-30b-a3b-t4k", (3, 5))
+    _full_size("qwen3-30b-a3b-t4k", (3, 5), every=True)
 
 
 def test_full_size_qwen3_t4k_compacted(dev):
-    _full_size("qwen3-30b-a3b-t4k", (3, 5), gathered=False)
+    _full_size("qwen3-30b-a3b-t4k", (3, 5), gathered=False, every=True)
 
 
 def test_full_size_qwen3_t32k(dev):
-    pipe = _full_size("qwen3-30b-a3b-t32k", (1, 2))
+    pipe = _full_size("qwen3-30b-a3b-t32k", (1, 2), every=True)
     counts = to_np(pipe.counts)
     assert counts.max() > 10 * counts.mean()
 
 
 @pytest.mark.parametrize("rate", [(1, 4), (1, 2), (1, 1)])
 def test_full_size_glm45_sweep(dev, rate):
-    pipe = _full_size("glm45-106b-a12b-t16k", rate)
+    # every expert and token where the FP64 oracle takes seconds (rho <= 1/2),
+    # sampled ones at rho = 1
+    pipe = _full_size("glm45-106b-a12b-t16k", rate, every=rate != (1, 1))
     if rate == (1, 1):
         N = pipe.N
         assert torch.equal(pipe.sel_pos[:N].long(), torch.arange(N, device=dev))
@@ -416,7 +439,7 @@ def test_full_size_glm45_sweep(dev, rate):
 
 def test_full_size_stress(dev):
     cfg = get_config("stress-e256")
-    pipe = _full_size("stress-e256", (1, 2), cap=cfg.cap)
+    pipe = _full_size("stress-e256", (1, 2), cap=cfg.cap, every=True)
     q = to_np(pipe.quota)
     assert q.max() == cfg.cap
 
