@@ -947,8 +947,9 @@ def run_reference(args, rank: int):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "T": cfg.T, "D": cfg.D, "H": cfg.H, "E": cfg.E,
-                   "K": cfg.K, "rho": f"{rate[0]}/{rate[1]}", "sampled_tokens": small.T},
+        "config": {"workload": f"{cfg.name} rho={rate[0]}/{rate[1]}", "layer": cfg.name,
+                   "T": cfg.T, "D": cfg.D, "H": cfg.H, "E": cfg.E, "K": cfg.K,
+                   "rho": f"{rate[0]}/{rate[1]}", "sampled_tokens": small.T},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": f"a {small.T}-token layer of {cfg.name}'s recipe per "
