@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace lrm {
 
@@ -339,6 +340,54 @@ __global__ void clear_header_kernel(int32_t* w) {
   if (threadIdx.x < kWsHeaderWords) w[threadIdx.x] = 0;
 }
 
+// One launch of the single-cluster dispatch (N <= dispatch_fused_max_pairs()):
+// needs no workspace; expert ids outside [0, E) are clamped and flag
+// LRM_DEVERR_EXPERT_ID in *err (err may be null).
+lrm_status launch_dispatch_fused(const int32_t* topk_idx, int64_t N, int E, int32_t* perm,
+                                 int32_t* inv, int32_t* counts, int32_t* off, int32_t* err,
+                                 cudaStream_t cs) {
+  const size_t shf = ((size_t)kFusedWarps * E + 2 * E) * 4;
+  if (shf > 48 * 1024 &&
+      cudaFuncSetAttribute(dispatch_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)shf) != cudaSuccess) {
+    (void)cudaGetLastError();  // leave no error behind for a later call to report
+    return LRM_ERR_CUDA;
+  }
+  // 16 CTAs (twice the SMs) where a 16-CTA cluster of this kernel fits
+  // the GPU, else the portable 8
+  int nctas = kFusedCtas;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = shf;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = LRM_PDL ? 2 : 1;
+  if (cudaFuncSetAttribute(dispatch_fused_kernel,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cfg.gridDim = dim3(kFusedCtasMax);
+    attr[0].val.clusterDim.x = kFusedCtasMax;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, dispatch_fused_kernel, &cfg) == cudaSuccess &&
+        clusters >= 1)
+      nctas = kFusedCtasMax;
+  }
+  (void)cudaGetLastError();  // a refused query leaves the portable size
+  cfg.gridDim = dim3(nctas);
+  attr[0].val.clusterDim.x = nctas;
+  if (cudaLaunchKernelEx(&cfg, dispatch_fused_kernel, topk_idx, N, E, perm, inv, counts, off,
+                         err) != cudaSuccess)
+    return LRM_ERR_CUDA;
+  return launch_status();
+}
+
+int64_t dispatch_fused_max_pairs() { return kFusedMaxPairs; }
+
 }  // namespace lrm
 
 using namespace lrm;
@@ -390,46 +439,8 @@ extern "C" lrm_status lrm_dispatch_permute(const lrm_shape* s, const int32_t* to
     return LRM_ERR_INVALID_ARG;
   cudaStream_t cs = (cudaStream_t)stream;
   const int E = s->E;
-  if (N <= kFusedMaxPairs) {
-    const size_t shf = ((size_t)kFusedWarps * E + 2 * E) * 4;
-    if (shf > 48 * 1024 &&
-        cudaFuncSetAttribute(dispatch_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)shf) != cudaSuccess) {
-      (void)cudaGetLastError();  // leave no error behind for a later call to report
-      return LRM_ERR_CUDA;
-    }
-    // 16 CTAs (twice the SMs) where a 16-CTA cluster of this kernel fits
-    // the GPU, else the portable 8
-    int nctas = kFusedCtas;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kFusedThreads);
-    cfg.dynamicSmemBytes = shf;
-    cfg.stream = cs;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = LRM_PDL ? 2 : 1;
-    if (cudaFuncSetAttribute(dispatch_fused_kernel,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-      cfg.gridDim = dim3(kFusedCtasMax);
-      attr[0].val.clusterDim.x = kFusedCtasMax;
-      int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, dispatch_fused_kernel, &cfg) == cudaSuccess &&
-          clusters >= 1)
-        nctas = kFusedCtasMax;
-    }
-    (void)cudaGetLastError();  // a refused query leaves the portable size
-    cfg.gridDim = dim3(nctas);
-    attr[0].val.clusterDim.x = nctas;
-    if (cudaLaunchKernelEx(&cfg, dispatch_fused_kernel, topk_idx, N, E, perm, inv, counts, off,
-                           error_word(ws)) != cudaSuccess)
-      return LRM_ERR_CUDA;
-    return launch_status();
-  }
+  if (N <= kFusedMaxPairs)
+    return launch_dispatch_fused(topk_idx, N, E, perm, inv, counts, off, error_word(ws), cs);
   const int nblk = dispatch_chunks(N);
   int32_t* chunk_hist = reinterpret_cast<int32_t*>((char*)ws + kWsHeaderBytes);
   int32_t* chunk_rel = chunk_hist + (int64_t)E * nblk;

@@ -11,11 +11,13 @@
 // instead, which every GPU that loads the library holds until the process
 // exits.
 //
-// The kernels are the ones lrm_dispatch_permute launches; only where their
-// scratch lives differs.
+// The kernels are the ones lrm_dispatch_permute launches: up to the
+// single-launch limit the one-cluster kernel, which needs no scratch at all;
+// above it the three launches, whose tables live in the array below.
 #include <mutex>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace lrm {
 
@@ -72,6 +74,9 @@ extern "C" lrm_status lrm_dispatch_permute_noalloc(const lrm_shape* s, const int
   const int E = s->E;
   const int64_t nblk = N > 0 ? (N + kChunkPairs - 1) / kChunkPairs : 1;
   if ((int64_t)E * nblk > LRM_NOALLOC_MAX_CHUNK_ENTRIES) return LRM_ERR_WORKSPACE;
+  if (N <= dispatch_fused_max_pairs())  // one launch, no tables
+    return launch_dispatch_fused(topk_idx, N, E, perm, inv, counts, off, dev_err,
+                                 (cudaStream_t)stream);
   int32_t* scratch = nullptr;
   if ((st = scratch_for_current_device(&scratch)) != LRM_OK) return st;
   // Both tables are written in full before they are read, so the previous

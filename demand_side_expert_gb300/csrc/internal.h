@@ -58,6 +58,12 @@ lrm_status launch_fwd_tc(const FwdArgs& a, unsigned parts);
 lrm_status launch_fwd_f32(const FwdArgs& a, unsigned parts);
 // Bounded-wait self-test of the grouped GEMM pipeline (see lrm.h).
 lrm_status selftest_wait_timeout(void* ws, size_t ws_bytes, cudaStream_t cs);
+// Dispatch permutation in one launch of one thread-block cluster, for up to
+// dispatch_fused_max_pairs() pairs; no workspace (dispatch.cu).
+lrm_status launch_dispatch_fused(const int32_t* topk_idx, int64_t N, int E, int32_t* perm,
+                                 int32_t* inv, int32_t* counts, int32_t* off, int32_t* err,
+                                 cudaStream_t cs);
+int64_t dispatch_fused_max_pairs();
 // dx[t] = sum over kept slots of dx_c rows (deterministic, no atomics).
 lrm_status launch_dx_gather(const lrm_shape* s, const float* dx_c, const int32_t* inv,
                             const int32_t* row_of_pos, float* dx, int32_t* err,

@@ -275,18 +275,21 @@ lrm_status lrm_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
  * handed only their input and output tensors, e.g. a plugin inside a host
  * whose memory manager owns the whole device budget; a cudaMalloc there
  * would bypass that accounting and can stall the whole device. This entry
- * point allocates nothing: its per-chunk tables live in one file-scope
- * device array of 2 * LRM_NOALLOC_MAX_CHUNK_ENTRIES int32 (512 KiB), which
- * every GPU that loads the library holds until the process exits.
+ * point allocates nothing. Up to 2^17 routed pairs it runs the one-cluster
+ * dispatch, which needs no scratch; above that, the per-chunk tables of the
+ * three-launch dispatch live in one file-scope device array of
+ * 2 * LRM_NOALLOC_MAX_CHUNK_ENTRIES int32 (512 KiB), which every GPU that
+ * loads the library holds until the process exits.
  *  - Same outputs as lrm_dispatch_permute (bit for bit). dev_err may be
  *    NULL; otherwise LRM_DEVERR_EXPERT_ID is ORed into *dev_err (a 4-byte
  *    device word the caller clears).
  *  - Limit: E * ceil(T*K / 2048) <= LRM_NOALLOC_MAX_CHUNK_ENTRIES, else
  *    LRM_ERR_WORKSPACE is returned before anything is launched (the built-in
  *    scratch is too small; use lrm_dispatch_permute with a workspace).
- *  - The first call on each device looks up the array's device address with
- *    cudaGetSymbolAddress (once, with that device current); make that first
- *    call before any stream capture.
+ *  - The first call on each device that needs the array (more than 2^17
+ *    pairs) looks up its device address with cudaGetSymbolAddress (once,
+ *    with that device current); make that first call before any stream
+ *    capture.
  *  - All calls share the one array: calls whose kernels overlap on the GPU
  *    (different streams, or several host threads) race and corrupt each
  *    other's results; serialise them. Every table entry a call reads is

@@ -34,8 +34,8 @@ def _reference(lrm, shape, idx, N, E, dev):
 
 
 @pytest.mark.parametrize("name,over", [
-    ("qwen3-30b-a3b-t4k", {}),                      # 32768 pairs, 128 experts
-    ("stress-e256", {"D": 64, "H": 64}),            # 262144 pairs, 256 experts
+    ("qwen3-30b-a3b-t4k", {}),                      # 32768 pairs: one cluster, no table
+    ("stress-e256", {"D": 64, "H": 64}),            # 262144 pairs, 256 experts: the tables
     ("tiny", {}),
 ])
 def test_noalloc_dispatch_matches_workspace_dispatch_twice(name, over):
@@ -57,14 +57,15 @@ def test_noalloc_dispatch_matches_workspace_dispatch_twice(name, over):
             assert torch.equal(a[:n], b[:n])
 
 
-def test_noalloc_dispatch_with_1024_experts():
-    """1024 experts: the count and scatter kernels need more than 48 KiB of
-    shared memory, so the call first raises their limit; the result is the
-    workspace dispatch's (its single-cluster kernel) bit for bit, twice."""
+def test_noalloc_dispatch_with_1000_experts():
+    """1000 experts and 133,120 pairs (65 chunks, above the single-launch
+    limit): the count and scatter kernels need more than 48 KiB of shared
+    memory, so the call first raises their limit; the result is the workspace
+    dispatch's bit for bit, twice."""
     from demand_side_expert_gb300 import lrm
 
     dev = torch.device("cuda:0")
-    cfg = get_config("qwen3-30b-a3b-t4k", T=1024, D=64, H=64, E=1024, K=8)
+    cfg = get_config("qwen3-30b-a3b-t4k", T=16640, D=64, H=64, E=1000, K=8)
     N, E = cfg.N, cfg.E
     shape = lrm.make_shape(cfg.T, cfg.D, cfg.H, cfg.E, cfg.K, lrm.LRM_BF16)
     idx = generate(cfg, device=dev)["topk_idx"]
