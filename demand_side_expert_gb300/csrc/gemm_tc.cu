@@ -97,6 +97,20 @@ constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 
 enum Mode { kG1 = 0, kG2 = 1, kG3 = 2, kG4 = 3, kF1 = 4, kF2 = 5 };
 
+// Wide tiles (W): a data-gradient product on CTA pairs whose tile is 256 rows
+// by 512 columns. One A tile feeds two 256-column accumulators, so a CTA takes
+// in 24 KB of operands per 128 x 256 x 64 block of MMA work instead of 32 KB,
+// and each ring stage carries eight MMAs; but both accumulators then belong to
+// one tile, whose epilogue no longer overlaps the next tile's MMAs. FC1 dgrad
+// runs wide when its K extent is long (wide_fc1_dgrad).
+template <int MODE, bool PAIR, bool W>
+struct Ring {
+  static constexpr bool kWide = W && PAIR && (MODE == kG1 || MODE == kG4);
+  static constexpr uint32_t kBBytes = Cfg<PAIR>::kBRows * BK * 2;  // one B box of a CTA
+  static constexpr uint32_t kStageBytes = A_BYTES + (kWide ? 2 : 1) * kBBytes;  // 32-48 KB
+  static constexpr int kTileCols = kWide ? 2 * BN : BN;  // output columns of a tile
+};
+
 // Operand maps (A, B, second B for G4 and F1) and output maps (G2: dW_down,
 // G3: dW_gate and dW_up, G4: dx_c), passed by value in parameter space.
 struct Maps {
@@ -458,6 +472,7 @@ struct Sched {
   const int* tpre;   // dgrad: [E+1] tile prefix
   const int* order;  // wgrad: experts by retained rows, descending
   int E, ntn, mtiles, kdim_blocks, total, tm;  // tm: rows of a unit's tile (128 or 256)
+  int tn;                                      // dgrad: output columns of a tile (256 or 512)
 };
 
 template <int MODE>
@@ -484,7 +499,7 @@ __device__ __forceinline__ Tile decode(const Sched& s, int tau, int rank) {
     const int loc = tau - s.tpre[lo];
     const int mt = loc / s.ntn;
     t.m0 = s.goff[lo] + mt * s.tm;
-    t.n0 = (loc % s.ntn) * BN;
+    t.n0 = (loc % s.ntn) * s.tn;
     t.valid = min(s.tm, s.goff[lo + 1] - t.m0);
     t.nkb = s.kdim_blocks;
     t.row0 = 0;
@@ -549,14 +564,17 @@ __device__ __forceinline__ void swiglu_chunk(const uint32_t (&r)[32], const uint
 //   block whose last 16-row slice crosses the group end is the exception: the
 //   odd CTA's copy lands on its own full barrier, its (otherwise idle) MMA warp
 //   zeroes the rows past the group end and then arrives on the even CTA's.
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool W>
 __global__ void __launch_bounds__(Threads<MODE, PAIR>::kCount, 1)
 grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   constexpr int NT = Threads<MODE, PAIR>::kCount;
   constexpr int NG = Threads<MODE, PAIR>::kGather;
   constexpr bool WG = Geo<MODE>::kWgrad;
   constexpr int BNL = Cfg<PAIR>::kBRows;
-  constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
+  constexpr bool WIDE = Ring<MODE, PAIR, W>::kWide;
+  constexpr uint32_t STB = Ring<MODE, PAIR, W>::kStageBytes;
+  constexpr uint32_t BBOX = Ring<MODE, PAIR, W>::kBBytes;
+  constexpr int TN = Ring<MODE, PAIR, W>::kTileCols;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -589,6 +607,10 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const bool queued = WG && !PAIR && LRM_TC_WG_QUEUE && p.queue != nullptr;
+  // wide tiles: output columns of the product; a tile's second accumulator
+  // (columns n0 + 256 ...) is skipped, copies and MMAs, when none of its
+  // columns exist
+  const int dg_cols = MODE == kG1 ? p.H : p.D;
   // warps that read every tile id: MMA, epilogue, and the gather warps at work
   const int gathering = (NG > 0 && p.a_rows && !p.selftest) ? min(NG, STAGES) : 0;
 
@@ -660,11 +682,12 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
   sc.goff = goff;
   sc.E = E;
   sc.tm = Cfg<PAIR>::kTileRows;
+  sc.tn = TN;
   if constexpr (MODE == kG1) {
-    sc.ntn = (p.H + BN - 1) / BN;
+    sc.ntn = (p.H + TN - 1) / TN;
     sc.kdim_blocks = p.D / BK;
   } else if constexpr (MODE == kG4) {
-    sc.ntn = (p.D + BN - 1) / BN;
+    sc.ntn = (p.D + TN - 1) / TN;
     sc.kdim_blocks = 2 * p.H / BK;
   } else if constexpr (MODE == kF1) {
     sc.ntn = (p.H + BN / 2 - 1) / (BN / 2);
@@ -799,6 +822,8 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       };
       for (int ri = 0, tau = next(0); tau < sc.total; tau = stop ? sc.total : next(++ri)) {
         const Tile t = decode<MODE>(sc, tau, rank);
+        const bool two = WIDE && t.n0 + BN < dg_cols;
+        const uint32_t stb = (WIDE && !two) ? STB - BBOX : STB;  // bytes one CTA copies
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_ns)) {
             stop = true;
@@ -820,8 +845,8 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (!to_leader)
             mbar_expect_tx(&full[stage],
                            gathered_a                       ? STB - A_BYTES
-                           : (PAIR && leader && !tailz)     ? 2 * STB - (odd_idle ? A_BYTES : 0)
-                                                            : STB);
+                           : (PAIR && leader && !tailz)     ? 2 * stb - (odd_idle ? A_BYTES : 0)
+                                                            : stb);
           auto load2 = [&](uint8_t* dst, const CUtensorMap* m, int x, int y) {
             if (to_leader) tma_load_2d_pair(dst, m, bar_cl, x, y);
             else tma_load_2d(dst, m, &full[stage], x, y);
@@ -834,11 +859,14 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if constexpr (MODE == kG1) {
             if (leader || !odd_idle) load2(a_s, mapA, kb * BK, t.cm0);
             load3(b_s, mapB, kb * BK, nb0, t.e);
+            if (WIDE && two) load3(b_s + BBOX, mapB, kb * BK, nb0 + BN, t.e);
           } else if constexpr (MODE == kG4) {
             if (leader || !odd_idle) load2(a_s, mapA, kb * BK, t.cm0);
             const int hb = p.H / BK;
-            if (kb < hb) load3(b_s, mapB, kb * BK, nb0, t.e);
-            else load3(b_s, mapB2, (kb - hb) * BK, nb0, t.e);
+            const CUtensorMap* mb = kb < hb ? mapB : mapB2;
+            const int kx = (kb < hb ? kb : kb - hb) * BK;
+            load3(b_s, mb, kx, nb0, t.e);
+            if (WIDE && two) load3(b_s + BBOX, mb, kx, nb0 + BN, t.e);
           } else if constexpr (MODE == kF1) {
             // tile columns [0, 128): gate h0.., [128, 256): up h0..; 64 x 64 boxes
             if (leader || !odd_idle) load2(a_s, mapA, kb * BK, t.cm0);
@@ -912,8 +940,11 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       const Tile t = decode<MODE>(sc, tau, rank);
       if (t.nkb <= 0) continue;
       if (!warp_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, p.wait_ns)) break;
+      // a wide tile fills both accumulators (acc is then always 0)
+      if (WIDE && !warp_wait(&tempty[1], acc_phase ^ 1, abort_flag, p.err, p.wait_ns)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
+      const bool two = WIDE && t.n0 + BN < dg_cols;
       for (int kb = 0; kb < t.nkb; ++kb) {
         if (!warp_wait(&full[stage], phase, abort_flag, p.err, p.wait_ns)) {
           stop = true;
@@ -945,6 +976,12 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
             const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
             if constexpr (PAIR) umma_bf16_pair(d_tmem, ad[ks], bd[ks], idesc, accum);
             else umma_bf16(d_tmem, ad[ks], bd[ks], idesc, accum);
+            if constexpr (WIDE) {
+              // the second accumulator: same A slice, the second B box (its
+              // descriptor differs from the first by the box's offset >> 4)
+              if (two)
+                umma_bf16_pair(d_tmem + BN, ad[ks], bd[ks] + (BBOX >> 4), idesc, accum);
+            }
           };
           if (nks == BK / 16) {  // a whole K block: the four MMAs back to back
 #pragma unroll
@@ -968,10 +1005,15 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       if (lane == 0) {
         if constexpr (PAIR) umma_commit_pair(&tfull[acc], 3);
         else umma_commit(&tfull[acc]);
+        if constexpr (WIDE) umma_commit_pair(&tfull[1], 3);
       }
       __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if constexpr (WIDE) {
+        acc_phase ^= 1;
+      } else {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
     }
     // all MMAs of this CTA (pair) must finish before TMEM is released
     if (issued_any && lane == 0) {
@@ -1102,10 +1144,11 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
     };
 
     for (int ri = 0, tau = tile_of(0); tau < sc.total; tau = tile_of(++ri)) {
-      const Tile t = decode<MODE>(sc, tau, rank);
-      if (t.nkb <= 0) {
+      const Tile t0 = decode<MODE>(sc, tau, rank);
+      if (t0.nkb <= 0) {
         // expert without retained rows: its weight gradient is zero
         if constexpr (WG) {
+          const Tile& t = t0;
           if (t.cm0 + q * 32 < row_lim) {
             uint32_t z[32];
 #pragma unroll
@@ -1116,7 +1159,16 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         }
         continue;
       }
-      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns)) break;
+      bool quit = false;
+      // one accumulator per 256 columns: a wide tile's second one holds
+      // columns n0 + 256 ...
+      for (int half = 0; half < (WIDE ? 2 : 1); ++half) {
+      Tile t = decode<MODE>(sc, tau, rank);  // (decoded again: keeps t0 out of registers)
+      t.n0 += half * BN;
+      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns)) {
+        quit = true;
+        break;
+      }
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if constexpr (MODE == kG1) {
@@ -1334,6 +1386,8 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+      }
+      if (quit) break;
     }
     if (lane == 0) bulk_wait_all();  // staged stores done before smem goes away
     __syncwarp();
@@ -1431,9 +1485,9 @@ static size_t smem_bytes(int E, int stages, uint32_t stage_bytes, int stage_bufs
 #define LRM_TC_WG_STAGE_BUFS 1
 #endif
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool W = false>
 static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStream_t cs) {
-  constexpr uint32_t STB = Cfg<PAIR>::kStageBytes;
+  constexpr uint32_t STB = Ring<MODE, PAIR, W>::kStageBytes;
   // forward: a, b and phi blocks (F1) or y blocks (F2) for the staged stores
   p.stage_bufs = Geo<MODE>::kFwd ? (LRM_TC_FWD_STAGED ? (MODE == kF1 ? 2 : 1) : 0)
                  : Geo<MODE>::kWgrad                ? LRM_TC_WG_STAGE_BUFS
@@ -1442,7 +1496,7 @@ static lrm_status launch_mode(const Maps& maps, Params p, int64_t tiles, cudaStr
   while (p.stages > 2 && smem_bytes(p.E, p.stages, STB, p.stage_bufs) > kSmemLimit) --p.stages;
   const size_t smem = smem_bytes(p.E, p.stages, STB, p.stage_bufs);
   if (smem > kSmemLimit) return LRM_ERR_UNSUPPORTED;
-  auto kern = grouped_gemm_kernel<MODE, PAIR>;
+  auto kern = grouped_gemm_kernel<MODE, PAIR, W>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return LRM_ERR_CUDA;
@@ -1490,6 +1544,16 @@ static lrm_status launch_any(const Maps& single, const Maps& pair, const Params&
     return launch_mode<MODE, true>(pair, p, tiles_pair, cs);
   else
     return launch_mode<MODE, false>(single, p, tiles_single, cs);
+}
+
+// FC1 dgrad runs on wide tiles when its K extent (2H) spans at least this many
+// 64-deep blocks: measured 2-4% faster at 2H = 2,816 (44 blocks), 2-3% slower
+// at 2H = 1,536 (24 blocks), where the exposed epilogue weighs more. (FC2
+// dgrad, whose epilogue also reads the saved [a | b] rows, measured 10-40%
+// slower on wide tiles.)
+constexpr int kWideMinKBlocks = 32;
+static bool wide_fc1_dgrad(int H) {
+  return ((LRM_TC_PAIR_MODES >> kG4) & 1) != 0 && 2 * H / BK >= kWideMinKBlocks;
 }
 
 // Weight-gradient products with gathered A rows run on single CTAs (the
@@ -1629,9 +1693,10 @@ lrm_status launch_bwd_tc(const BwdArgs& a, unsigned parts) {
     m2.o1 = m2.o2 = m1.o1;
     p.out0 = a.dx_c;
     p.out1 = nullptr;
-    if ((st = launch_any<kG4>(m1, m2, p, dg_tiles(BM, D), dg_tiles(2 * BM, D), a.stream)) !=
-        LRM_OK)
-      return st;
+    st = wide_fc1_dgrad(H)
+             ? launch_mode<kG4, true, true>(m2, p, dg_tiles(2 * BM, D), a.stream)
+             : launch_any<kG4>(m1, m2, p, dg_tiles(BM, D), dg_tiles(2 * BM, D), a.stream);
+    if (st != LRM_OK) return st;
   }
   return st;
 }

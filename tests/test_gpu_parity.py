@@ -87,6 +87,17 @@ def test_bf16_ragged_tiles(dev, rate):
     full_parity(cfg, dev, rate)
 
 
+@pytest.mark.parametrize("rate", [(1, 2), (1, 1)])
+@pytest.mark.parametrize("gathered", [False, True])
+def test_fc1_dgrad_on_wide_tiles(dev, rate, gathered):
+    # 2H = 2048 spans 32 K blocks: FC1 dgrad runs on 256 x 512 tiles. D = 640
+    # ends in a tile whose first accumulator is partly outside D and whose
+    # second lies wholly outside it (its copies and MMAs are skipped); the
+    # smaller experts' tiles leave the odd CTA of a pair without rows.
+    cfg = get_config("glm45-106b-a12b-t16k", T=1024, D=640, H=1024, E=12, K=3)
+    full_parity(cfg, dev, rate, gathered=gathered)
+
+
 def test_bf16_wide_layer_many_experts(dev):
     cfg = get_config("glm45-106b-a12b-t16k", T=768, D=512, H=320, E=24, K=4)
     full_parity(cfg, dev, (3, 4))
