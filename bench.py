@@ -401,6 +401,53 @@ def time_layer(pipe, inp, ab, phi, rate, cfg, flush, stream, steps, warmup, gath
             "wall": wall}
 
 
+# HBM-bound segments that also get a size-matched copy: the same bytes moved by
+# a plain device-to-device copy (half read, half written), timed the same way
+COPY_MATCHED = ("score", "compact", "scatter_dx")
+
+
+def size_matched_copies(cfg, M: int, gathered: bool, flush, stream, reps: int = 10) -> dict:
+    """For each segment in COPY_MATCHED: the mean time of a device-to-device
+    copy that moves that segment's algorithmic bytes, with the L2 flushed
+    before each copy and CUDA events around the copy alone. The measured copy
+    peak is taken on gigabytes; a launch that moves tens of megabytes spends a
+    visible share of its time in launch, ramp-up and drain, which this copy
+    shows at the segment's own size."""
+    import torch
+
+    alg = algorithmic(cfg, M, gathered)
+    out = {}
+    for seg in COPY_MATCHED:
+        nbytes = alg[seg]["bytes"]
+        half = max(16, (nbytes // 2) // 16 * 16)
+        src = torch.ones(half, dtype=torch.uint8, device=flush.device)
+        dst = torch.empty_like(src)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 3):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dst.copy_(src)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1))
+        ms = statistics.mean(times)
+        out[seg] = {"bytes": 2 * half, "ms": round(ms, 4),
+                    "gbs": round(2 * half / (ms * 1e-3) / 1e9, 1)}
+        del src, dst
+    return out
+
+
+def attach_copies(summary: dict, copies: dict) -> None:
+    for seg, c in copies.items():
+        k = summary["kernels"][seg]
+        k["size_matched_copy"] = c
+        k["frac_size_matched_copy"] = round(k["gbs"] / c["gbs"], 4) if c["gbs"] else None
+
+
 def largest_segment(pipe) -> int:
     return int(pipe.counts.max().item()) if pipe.E else 0
 
@@ -538,6 +585,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    gathered, dist)
     n_max = largest_segment(pipe)
     M = t["M"]
+    copies = size_matched_copies(cfg, M, gathered, flush, stream)
     total_s = sum(t["step_ms"]) / 1e3
     total_max, rows_sum = aggregate_ranks(total_s, M * args.steps, dev, dist)
     peaks = load_peaks()
@@ -587,6 +635,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             ot = time_layer(opipe, oinp, oab, ophi, orate, ocfg, flush, stream, args.steps,
                             args.warmup, gathered)
             sm = layer_summary(ocfg, orate, ot, peaks, gathered, largest_segment(opipe))
+            attach_copies(sm, size_matched_copies(ocfg, ot["M"], gathered, flush, stream))
             sm["workload"] = ocfg.name
             sm["T"], sm["D"], sm["H"], sm["E"], sm["K"] = ocfg.T, ocfg.D, ocfg.H, ocfg.E, ocfg.K
             sm["quota_cap"] = ocfg.cap
@@ -600,6 +649,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         return None
 
     head = layer_summary(cfg, rate, t, peaks, gathered, n_max)
+    attach_copies(head, copies)
     line = {
         "metric": METRIC,
         "value": round(rows_sum / total_max, 1),
