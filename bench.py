@@ -50,8 +50,8 @@ SEGMENTS = ["dispatch", "score", "select", "compact", "fc2_dgrad", "fc2_wgrad",
 KERNEL_NAMES = {
     "dispatch": "dispatch_fused_kernel",
     "score": "score_kernel", "select": "select_kernel", "compact": "compact_kernel",
-    "fc2_dgrad": "grouped_gemm_kernel<0, 1>", "fc2_wgrad": "grouped_gemm_kernel<1, 0>",
-    "fc1_wgrad": "grouped_gemm_kernel<2, 0>", "fc1_dgrad": "grouped_gemm_kernel<3, 1>",
+    "fc2_dgrad": "grouped_gemm_kernel<0, 1, 0>", "fc2_wgrad": "grouped_gemm_kernel<1, 0, 0>",
+    "fc1_wgrad": "grouped_gemm_kernel<2, 0, 0>", "fc1_dgrad": "grouped_gemm_kernel<3, 1, 0>",
     "scatter_dx": "dx_gather_kernel",
 }
 FUSED_DISPATCH_MAX_PAIRS = 1 << 17  # above it dispatch takes three launches
@@ -59,15 +59,30 @@ FUSED_DISPATCH_MAX_PAIRS = 1 << 17  # above it dispatch takes three launches
 FWD_SEGMENTS = ["dispatch", "gather", "fc1_fwd", "fc2_fwd", "combine"]
 FWD_KERNEL_NAMES = {
     "dispatch": "dispatch_fused_kernel", "gather": "gather_tokens_kernel",
-    "fc1_fwd": "grouped_gemm_kernel<4, 1>", "fc2_fwd": "grouped_gemm_kernel<5, 1>",
+    "fc1_fwd": "grouped_gemm_kernel<4, 1, 0>", "fc2_fwd": "grouped_gemm_kernel<5, 1, 0>",
     "combine": "combine_kernel",
 }
 
 
-def segment_kernels(seg: str, N: int, fwd: bool = False) -> str:
+# FC1 dgrad runs on 256 x 512 tiles (third template argument 1) when 2H spans
+# at least this many 64-deep K blocks
+WIDE_FC1_DGRAD_MIN_KBLOCKS = 32
+
+
+def segment_kernels(seg: str, cfg, fwd: bool = False) -> str:
     """Kernel name(s) of a segment as the launch list shows them."""
-    if seg == "dispatch" and N > FUSED_DISPATCH_MAX_PAIRS:
+    if seg == "dispatch" and cfg.N > FUSED_DISPATCH_MAX_PAIRS:
         return "dispatch_hist_kernel + dispatch_scan_kernel + dispatch_scatter_kernel"
+    if seg == "fc1_dgrad" and not fwd and 2 * cfg.H // 64 >= WIDE_FC1_DGRAD_MIN_KBLOCKS:
+        return "grouped_gemm_kernel<3, 1, 1>"
+    if seg == "score" and cfg.dtype == "bf16" and cfg.K <= 8:
+        # BF16 layers: the instantiation with the fewest 16-byte chunks per lane
+        # (GV for a g row, HV for a phi row) that covers the row lengths
+        gl, hl = -(-cfg.D // 256), -(-cfg.H // 256)
+        for gv in (8, 16):
+            for hv in (1, 2, 3, 4, 6):
+                if gl <= gv and hl <= hv:
+                    return f"score_upfront_kernel<{gv}, {hv}>"
     return (FWD_KERNEL_NAMES if fwd else KERNEL_NAMES)[seg]
 
 
@@ -462,7 +477,7 @@ def layer_summary(cfg, rate, t: dict, peaks: dict, gathered: bool, n_max: int) -
     kernels = {}
     for s in SEGMENTS:
         ms = statistics.mean(seg_ms[s])
-        k = {"ms": round(ms, 4), "kernels": segment_kernels(s, cfg.N),
+        k = {"ms": round(ms, 4), "kernels": segment_kernels(s, cfg),
              "gbs": round(alg[s]["bytes"] / (ms * 1e-3) / 1e9, 1),
              "frac_hbm": round(alg[s]["bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
         if "flops" in alg[s]:
@@ -487,7 +502,7 @@ def layer_summary(cfg, rate, t: dict, peaks: dict, gathered: bool, n_max: int) -
     a = alg[dominant]
     roof = roofline_of(a, statistics.mean(seg_ms[dominant]), peaks)
     roof["traffic"] = traffic.get(dominant)
-    roof["kernel"] = KERNEL_NAMES[dominant]
+    roof["kernel"] = segment_kernels(dominant, cfg)
     roof["algorithmic_bytes"] = a["bytes"]
     if "flops" in a:
         roof["algorithmic_flops"] = a["flops"]
@@ -770,7 +785,7 @@ def run_recompute(pipe, inp, phi, rate, cfg, flush, stream, args):
     a = {"bytes": M * cfg.D * s + 2 * cfg.E * cfg.D * cfg.H * s + M * 2 * cfg.H * s,
          "flops": 4 * M * cfg.D * cfg.H}
     roof = roofline_of(a, rec_ms, load_peaks())
-    roof["kernel"] = "grouped_gemm_kernel<4, 1>"
+    roof["kernel"] = FWD_KERNEL_NAMES["fc1_fwd"]
     return {"metric": "retained rows through the backward step per second, [a | b] recomputed",
             "value": round(M / (ms * 1e-3), 1), "unit": "rows/s", "ms_per_step": round(ms, 4),
             "steps": args.steps, "saved_state_bytes_avoided": cfg.N * 2 * cfg.H * s,
@@ -820,7 +835,7 @@ def run_forward(pipe, inp, cfg, flush, stream, args):
     peaks = load_peaks()
     kernels = {}
     for s in FWD_SEGMENTS:
-        k = {"ms": round(seg[s], 4), "kernels": segment_kernels(s, cfg.N, fwd=True),
+        k = {"ms": round(seg[s], 4), "kernels": segment_kernels(s, cfg, fwd=True),
              "gbs": round(alg[s]["bytes"] / (seg[s] * 1e-3) / 1e9, 1)}
         if "flops" in alg[s]:
             k["tflops"] = round(alg[s]["flops"] / (seg[s] * 1e-3) / 1e12, 1)
