@@ -75,6 +75,14 @@ constexpr int kGatherWarps = 4;  // weight-gradient products: A rows gathered by
 #ifndef LRM_TC_WG_QUEUE
 #define LRM_TC_WG_QUEUE 1
 #endif
+// CTAs that take their tiles from the short end of the longest-first list: those
+// with blockIdx % 4 below this count (0: every CTA takes from the long end). A
+// quarter or half of the CTAs at the short end measured 3-7% slower on the
+// weight-gradient products of the large layers: the store-bound short tiles then
+// run beside the long ones, whose operand loads slow down under their stores.
+#ifndef LRM_TC_WG_TAIL_QUARTERS
+#define LRM_TC_WG_TAIL_QUARTERS 0
+#endif
 // forward products: full 32-row blocks of their bf16 outputs through staged
 // TMA stores (1) instead of 16-byte row stores (0)
 #ifndef LRM_TC_FWD_STAGED
@@ -140,7 +148,9 @@ struct Params {
   int a_src_rows, a_src_cols;
   int ab_src_rows;  // rows of the [a | b] source (bound for ab_rows)
   int32_t* err;
-  int32_t* queue;  // weight-gradient tile queue: [next position, CTAs done, tiles handed out]
+  // weight-gradient tile queue: [positions taken from the head | from the tail
+  // (one 64-bit word), CTAs done, tiles handed out]
+  int32_t* queue;
 };
 
 // ----------------------------------------------------------------------------
@@ -798,9 +808,21 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       bool stop = false;
       int handed = 0;        // tiles this CTA took from the queue
       bool drained = false;  // the queue ran out
+      // one take: a ticket and a position in one 64-bit atomic (low word: takes
+      // from the head, high word: takes from the tail); a take whose two
+      // counts already sum to the tile count finds the list exhausted, so the
+      // two ends never hand out the same position
+      const bool from_tail = (int)(blockIdx.x & 3) < LRM_TC_WG_TAIL_QUARTERS;
+      auto take = [&]() -> int {
+        const unsigned long long old = atomicAdd(
+            reinterpret_cast<unsigned long long*>(p.queue), from_tail ? (1ull << 32) : 1ull);
+        const long long h = (long long)(old & 0xffffffffull), tl = (long long)(old >> 32);
+        if (h + tl >= (long long)sc.total) return sc.total;
+        return from_tail ? (int)(sc.total - 1 - tl) : (int)h;
+      };
       // the position of the next tile, taken one tile ahead so that the
       // atomic's round trip overlaps the current tile's copies
-      int ahead = queued ? atomicAdd(p.queue, 1) : 0;
+      int ahead = queued ? take() : 0;
       auto next = [&](int r) -> int {
         if (!queued) return tile_of(r);
         const int slot = r % kTQ;
@@ -811,7 +833,7 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
           if (ahead >= 0 && ahead < sc.total) {
             tau = ahead;
             ++handed;
-            ahead = atomicAdd(p.queue, 1);
+            ahead = take();
           } else {
             drained = true;
           }
@@ -917,16 +939,17 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
         // this CTA takes no more tiles: the last CTA to get here checks that
         // every tile was handed out once and rewinds the queue for the next
         // launch (which reads it only after this grid has completed)
-        atomicAdd(p.queue + 2, handed);
+        atomicAdd(p.queue + 3, handed);
         __threadfence();
-        const int prev = atomicAdd(p.queue + 1, 1);
+        const int prev = atomicAdd(p.queue + 2, 1);
         if (prev < 0 || prev >= (int)gridDim.x) flag_error(p.err, LRM_DEVERR_QUEUE);
         if (prev == (int)gridDim.x - 1) {
           __threadfence();
-          if (atomicAdd(p.queue + 2, 0) != sc.total) flag_error(p.err, LRM_DEVERR_QUEUE);
+          if (atomicAdd(p.queue + 3, 0) != sc.total) flag_error(p.err, LRM_DEVERR_QUEUE);
           atomicExch(p.queue, 0);
           atomicExch(p.queue + 1, 0);
           atomicExch(p.queue + 2, 0);
+          atomicExch(p.queue + 3, 0);
         }
       }
     }

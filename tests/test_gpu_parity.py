@@ -257,12 +257,12 @@ def test_weight_gradient_queue_flags_a_bad_header_and_rewinds(dev):
     words = pipe.ws.view(torch.int32)
     run_gpu(pipe, inp, (1, 2), gathered=True)
     assert pipe.device_error() == 0
-    assert words[4:7].tolist() == [0, 0, 0]
+    assert words[4:8].tolist() == [0, 0, 0, 0]
     ref = [getattr(pipe, k).clone() for k in ("dw_gate", "dw_up", "dw_down", "dx")]
     words[4] = 3  # the queue would start past three tiles
     run_gpu(pipe, inp, (1, 2), gathered=True)
     assert pipe.device_error() & lrm.LRM_DEVERR_QUEUE
-    assert words[4:7].tolist() == [0, 0, 0]
+    assert words[4:8].tolist() == [0, 0, 0, 0]
     pipe.clear_device_error()
     run_gpu(pipe, inp, (1, 2), gathered=True)
     assert pipe.device_error() == 0
