@@ -98,6 +98,18 @@ def test_fc1_dgrad_on_wide_tiles(dev, rate, gathered):
     full_parity(cfg, dev, rate, gathered=gathered)
 
 
+@pytest.mark.parametrize("over,rate", [
+    # 2H = 2176: 34 K blocks, 17 from each of W_gate and W_up; D = 576: the
+    # second tile's first accumulator holds 64 valid columns and its second none
+    ({"T": 700, "D": 576, "H": 1088, "E": 5, "K": 2}, (2, 3)),
+    # D = 1088: three tiles across D, the last one's second accumulator 64
+    # columns wide; K = 4 slots, groups of 43 to 283 retained rows
+    ({"T": 900, "D": 1088, "H": 1024, "E": 9, "K": 4}, (1, 3)),
+])
+def test_fc1_dgrad_on_wide_tiles_ragged(dev, over, rate):
+    full_parity(get_config("glm45-106b-a12b-t16k", **over), dev, rate)
+
+
 def test_bf16_wide_layer_many_experts(dev):
     cfg = get_config("glm45-106b-a12b-t16k", T=768, D=512, H=320, E=24, K=4)
     full_parity(cfg, dev, (3, 4))
