@@ -103,7 +103,7 @@ def test_fc1_dgrad_on_wide_tiles(dev, rate, gathered):
     # second tile's first accumulator holds 64 valid columns and its second none
     ({"T": 700, "D": 576, "H": 1088, "E": 5, "K": 2}, (2, 3)),
     # D = 832: two tiles across D, the second one's second accumulator holds
-    # 64 valid columns; K = 4 slots, groups of 43 to 283 retained rows
+    # 64 valid columns; K = 4 slots, groups of 42 to 286 retained rows
     ({"T": 900, "D": 832, "H": 1024, "E": 9, "K": 4}, (1, 3)),
 ])
 def test_fc1_dgrad_on_wide_tiles_ragged(dev, over, rate):
