@@ -35,8 +35,10 @@
 //             as shared memory allows (at most 6), guarded by mbarriers;
 //   warp 1    allocates 512 TMEM columns, one elected lane issues
 //             tcgen05.mma (M=128, N=256, K=16) into one of two 256-column
-//             accumulators; tcgen05.commit frees smem stages and hands
-//             finished accumulators to the epilogue;
+//             accumulators (a wide tile, FC1 dgrad on long K, fills both:
+//             256 x 512 per CTA pair, two B boxes per 48 KB stage);
+//             tcgen05.commit frees smem stages and hands finished
+//             accumulators to the epilogue;
 //   warps 2-9 epilogue: tcgen05.ld rows out of TMEM (one row per thread,
 //             two warps per 32-lane quarter, each half of the columns);
 //             G1 fuses the SwiGLU gradient (saved a, b rows prefetched one
@@ -131,7 +133,7 @@ struct Params {
   int E, D, H;
   int n_rows;      // row capacity of the compacted buffers
   int stage_bufs;  // 32x32 fp32 staging blocks per epilogue warp (0 to 3)
-  int stages;      // depth of the operand ring (3 or 4)
+  int stages;      // depth of the operand ring (3 to 6, as shared memory allows)
   const int32_t* sel_off;
   const __nv_bfloat16* ab_c;
   __nv_bfloat16* dab_c;
