@@ -96,8 +96,7 @@ constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 template <bool PAIR>
 struct Cfg {
   static constexpr int kBRows = PAIR ? BN / 2 : BN;
-  static constexpr uint32_t kStageBytes = A_BYTES + kBRows * BK * 2;  // 32 or 48 KB
-  static constexpr int kTileRows = PAIR ? 2 * BM : BM;                // M of one MMA
+  static constexpr int kTileRows = PAIR ? 2 * BM : BM;  // M of one MMA
 };
 constexpr uint32_t BOX_BYTES = 64 * 64 * 2;  // one 64x64 MN-major box
 constexpr uint32_t TMEM_COLS = 2 * BN;

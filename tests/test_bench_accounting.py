@@ -101,3 +101,24 @@ def test_headline_rate_is_the_middle_of_a_sweep():
     assert bench.headline_rate(get_config("qwen3-30b-a3b-t4k"), A()) == (3, 5)
     A.rate = "3/4"
     assert bench.headline_rate(get_config("glm45-106b-a12b-t16k"), A()) == (3, 4)
+
+
+@pytest.mark.parametrize("name,score,fc1_dgrad,dispatch", [
+    ("qwen3-30b-a3b-t4k", "score_upfront_kernel<8, 3>", "grouped_gemm_kernel<3, 1, 0>",
+     "dispatch_fused_kernel"),
+    ("qwen3-30b-a3b-t32k", "score_upfront_kernel<8, 3>", "grouped_gemm_kernel<3, 1, 0>",
+     "dispatch_hist_kernel + dispatch_scan_kernel + dispatch_scatter_kernel"),
+    ("glm45-106b-a12b-t16k", "score_upfront_kernel<16, 6>", "grouped_gemm_kernel<3, 1, 1>",
+     "dispatch_fused_kernel"),
+    ("stress-e256", "score_upfront_kernel<8, 2>", "grouped_gemm_kernel<3, 1, 0>",
+     "dispatch_hist_kernel + dispatch_scan_kernel + dispatch_scatter_kernel"),
+])
+def test_segment_kernel_names_follow_the_launch_rules(name, score, fc1_dgrad, dispatch):
+    # the names the launch list shows: score instantiation by chunks per lane
+    # (D/8 and H/8 sixteen-byte chunks over 32 lanes), wide FC1 dgrad tiles when
+    # 2H spans 32 or more 64-deep K blocks, three dispatch launches above 2^17 pairs
+    cfg = get_config(name)
+    assert bench.segment_kernels("score", cfg) == score
+    assert bench.segment_kernels("fc1_dgrad", cfg) == fc1_dgrad
+    assert bench.segment_kernels("dispatch", cfg) == dispatch
+    assert bench.segment_kernels("fc1_wgrad", cfg) == "grouped_gemm_kernel<2, 0, 0>"
