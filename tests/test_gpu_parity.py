@@ -228,13 +228,18 @@ def test_full_retention_bitwise_equals_uncompacted_run(dev):
         assert torch.equal(outs[k], res[k]), k
 
 
-def test_deterministic_repeats(dev):
-    cfg = get_config("qwen3-30b-a3b-t4k", T=512, D=256, H=128, E=8, K=4)
+@pytest.mark.parametrize("name,over,gathered", [
+    ("qwen3-30b-a3b-t4k", {"T": 512, "D": 256, "H": 128, "E": 8, "K": 4}, False),
+    # wide FC1 dgrad tiles, the weight-gradient tile queue and the gather warps
+    ("glm45-106b-a12b-t16k", {"T": 1024, "D": 640, "H": 1024, "E": 12, "K": 3}, True),
+])
+def test_deterministic_repeats(dev, name, over, gathered):
+    cfg = get_config(name, **over)
     inp = _to(generate(cfg, device="cpu"), dev)
     pipe = _pipe(cfg, dev)
     first = None
     for _ in range(3):
-        run_gpu(pipe, inp, (3, 5))
+        run_gpu(pipe, inp, (3, 5), gathered=gathered)
         cur = [getattr(pipe, k).clone() for k in ("score", "sel_pos", "dw_gate", "dw_up",
                                                    "dw_down", "dx")]
         if first is None:
