@@ -1187,229 +1187,230 @@ grouped_gemm_kernel(const __grid_constant__ Maps maps, const Params p) {
       // one accumulator per 256 columns: a wide tile's second one holds
       // columns n0 + 256 ...
       for (int half = 0; half < (WIDE ? 2 : 1); ++half) {
-      Tile t = decode<MODE>(sc, tau, rank);  // (decoded again: keeps t0 out of registers)
-      t.n0 += half * BN;
-      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns)) {
-        quit = true;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-      if constexpr (MODE == kG1) {
-        bool rv = row_local < t.cvalid;
-        const int64_t j = (int64_t)t.cm0 + row_local;
-        int64_t src = j;  // row of the saved [a | b]
-        if (p.ab_rows && rv) {
-          src = p.ab_rows[j];
-          if (src < 0 || src >= p.ab_src_rows) {
-            flag_error(p.err, LRM_DEVERR_INDEX);
-            rv = false;
-          }
+        Tile t = decode<MODE>(sc, tau, rank);  // (decoded again: keeps t0 out of registers)
+        t.n0 += half * BN;
+        if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns)) {
+          quit = true;
+          break;
         }
-        const __nv_bfloat16* arow = p.ab_c + src * 2 * p.H;
-        __nv_bfloat16* drow = p.dab_c + j * 2 * p.H;
-        const bool g1_whole = q * 32 + 32 <= t.cvalid;  // warp-uniform
-        uint4 a_cur[4], b_cur[4], a_nxt[4], b_nxt[4];
-        auto load_ab = [&](int h, uint4 (&av)[4], uint4 (&bv)[4]) {
-          if (rv && h < p.H) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              // read-only path: a row's four 16-byte pieces share its L1 lines
-              av[v] = __ldg(reinterpret_cast<const uint4*>(arow + h + 8 * v));
-              bv[v] = __ldg(reinterpret_cast<const uint4*>(arow + p.H + h + 8 * v));
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+        if constexpr (MODE == kG1) {
+          bool rv = row_local < t.cvalid;
+          const int64_t j = (int64_t)t.cm0 + row_local;
+          int64_t src = j;  // row of the saved [a | b]
+          if (p.ab_rows && rv) {
+            src = p.ab_rows[j];
+            if (src < 0 || src >= p.ab_src_rows) {
+              flag_error(p.err, LRM_DEVERR_INDEX);
+              rv = false;
             }
           }
-        };
-        load_ab(t.n0 + c_lo, a_cur, b_cur);
+          const __nv_bfloat16* arow = p.ab_c + src * 2 * p.H;
+          __nv_bfloat16* drow = p.dab_c + j * 2 * p.H;
+          const bool g1_whole = q * 32 + 32 <= t.cvalid;  // warp-uniform
+          uint4 a_cur[4], b_cur[4], a_nxt[4], b_nxt[4];
+          auto load_ab = [&](int h, uint4 (&av)[4], uint4 (&bv)[4]) {
+            if (rv && h < p.H) {
 #pragma unroll
-        for (int c = c_lo; c < c_hi; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c, r);
-          if (c + 32 < c_hi) load_ab(t.n0 + c + 32, a_nxt, b_nxt);
-          tmem_ld_wait();
-          const int h = t.n0 + c;
-          if (g1_whole && h < p.H) {
-            // the warp's 32 rows lie inside the group: stage the da and db
-            // blocks (32 rows x 64 B each, 64-byte swizzle) and write them
-            // with two TMA bulk-tensor stores
-            uint4 dav[4], dbv[4];
-            swiglu_chunk(r, a_cur, b_cur, dav, dbv);
-            if (!rv) {
-#pragma unroll
-              for (int v = 0; v < 4; ++v) dav[v] = dbv[v] = make_uint4(0, 0, 0, 0);
-            }
-            if (lane == 0) bulk_wait_read(0);
-            __syncwarp();
-            const int sw = (lane >> 1) & 3;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              *reinterpret_cast<uint4*>(wst + lane * 64 + ((v ^ sw) << 4)) = dav[v];
-              *reinterpret_cast<uint4*>(wst + 2048 + lane * 64 + ((v ^ sw) << 4)) = dbv[v];
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&maps.o1, wst, h, t.cm0 + q * 32);
-              tma_store_2d(&maps.o1, wst + 2048, p.H + h, t.cm0 + q * 32);
-              bulk_commit();
-            }
-          } else if (rv && h < p.H) {  // block crossing the group end: row by row
-            uint4 dav[4], dbv[4];
-            swiglu_chunk(r, a_cur, b_cur, dav, dbv);
-            uint4* da_dst = reinterpret_cast<uint4*>(drow + h);
-            uint4* db_dst = reinterpret_cast<uint4*>(drow + p.H + h);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              da_dst[v] = dav[v];
-              db_dst[v] = dbv[v];
-            }
-          }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            a_cur[v] = a_nxt[v];
-            b_cur[v] = b_nxt[v];
-          }
-        }
-      } else if constexpr (MODE == kF1) {
-        // this warp's 64 gate columns and the matching 64 up columns
-        const bool rv = row_local < t.cvalid;
-        const int64_t j = (int64_t)t.cm0 + row_local;
-        const int hbase = ((warp - 2) >> 2) * (BN / 4);
-        // the warp's 32 rows inside the group (warp-uniform): a, b and phi go
-        // out as 32 x 32 blocks (64-byte swizzle) through TMA stores
-        const bool whole = LRM_TC_FWD_STAGED && q * 32 + 32 <= t.cvalid;
-#pragma unroll 1
-        for (int cc = 0; cc < BN / 4; cc += 32) {
-          const int hl = hbase + cc;
-          uint32_t ra[32], rb[32];
-          tmem_ld32(taddr + hl, ra);
-          tmem_ld32(taddr + BN / 2 + hl, rb);
-          tmem_ld_wait();
-          const int h = t.n0 / 2 + hl;
-          if (whole && h < p.H) {
-            uint4 av[4], bv[4], fv[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float a[8], b[8], f[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                a[u] = __uint_as_float(ra[8 * v + u]);
-                b[u] = __uint_as_float(rb[8 * v + u]);
-                f[u] = a[u] * __fdividef(1.0f, 1.0f + __expf(-a[u])) * b[u];
+              for (int v = 0; v < 4; ++v) {
+                // read-only path: a row's four 16-byte pieces share its L1 lines
+                av[v] = __ldg(reinterpret_cast<const uint4*>(arow + h + 8 * v));
+                bv[v] = __ldg(reinterpret_cast<const uint4*>(arow + p.H + h + 8 * v));
               }
-              av[v] = Vec16<__nv_bfloat16>::pack(a);
-              bv[v] = Vec16<__nv_bfloat16>::pack(b);
-              fv[v] = Vec16<__nv_bfloat16>::pack(f);
             }
-            // one set of blocks per warp: a second set costs a ring stage
-            // and measured slower
-            uint8_t* sb = wst;
-            if (lane == 0) bulk_wait_read(0);
-            __syncwarp();
-            const int sw = (lane >> 1) & 3;
+          };
+          load_ab(t.n0 + c_lo, a_cur, b_cur);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              *reinterpret_cast<uint4*>(sb + lane * 64 + ((v ^ sw) << 4)) = av[v];
-              *reinterpret_cast<uint4*>(sb + 2048 + lane * 64 + ((v ^ sw) << 4)) = bv[v];
-              if (p.ob1) *reinterpret_cast<uint4*>(sb + 4096 + lane * 64 + ((v ^ sw) << 4)) = fv[v];
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&maps.o1, sb, h, t.cm0 + q * 32);
-              tma_store_2d(&maps.o1, sb + 2048, p.H + h, t.cm0 + q * 32);
-              if (p.ob1) tma_store_2d(&maps.o2, sb + 4096, h, t.cm0 + q * 32);
-              bulk_commit();
-            }
-          } else if (rv && h < p.H) {
-            __nv_bfloat16* arow = p.ob0 + j * 2 * p.H;
-            uint4* a_dst = reinterpret_cast<uint4*>(arow + h);
-            uint4* b_dst = reinterpret_cast<uint4*>(arow + p.H + h);
-            uint4* f_dst = p.ob1 ? reinterpret_cast<uint4*>(p.ob1 + j * p.H + h) : nullptr;
+          for (int c = c_lo; c < c_hi; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c, r);
+            if (c + 32 < c_hi) load_ab(t.n0 + c + 32, a_nxt, b_nxt);
+            tmem_ld_wait();
+            const int h = t.n0 + c;
+            if (g1_whole && h < p.H) {
+              // the warp's 32 rows lie inside the group: stage the da and db
+              // blocks (32 rows x 64 B each, 64-byte swizzle) and write them
+              // with two TMA bulk-tensor stores
+              uint4 dav[4], dbv[4];
+              swiglu_chunk(r, a_cur, b_cur, dav, dbv);
+              if (!rv) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float a[8], b[8], f[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                a[u] = __uint_as_float(ra[8 * v + u]);
-                b[u] = __uint_as_float(rb[8 * v + u]);
-                f[u] = a[u] * __fdividef(1.0f, 1.0f + __expf(-a[u])) * b[u];
+                for (int v = 0; v < 4; ++v) dav[v] = dbv[v] = make_uint4(0, 0, 0, 0);
               }
-              a_dst[v] = Vec16<__nv_bfloat16>::pack(a);
-              b_dst[v] = Vec16<__nv_bfloat16>::pack(b);
-              if (f_dst) f_dst[v] = Vec16<__nv_bfloat16>::pack(f);
+              if (lane == 0) bulk_wait_read(0);
+              __syncwarp();
+              const int sw = (lane >> 1) & 3;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                *reinterpret_cast<uint4*>(wst + lane * 64 + ((v ^ sw) << 4)) = dav[v];
+                *reinterpret_cast<uint4*>(wst + 2048 + lane * 64 + ((v ^ sw) << 4)) = dbv[v];
+              }
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&maps.o1, wst, h, t.cm0 + q * 32);
+                tma_store_2d(&maps.o1, wst + 2048, p.H + h, t.cm0 + q * 32);
+                bulk_commit();
+              }
+            } else if (rv && h < p.H) {  // block crossing the group end: row by row
+              uint4 dav[4], dbv[4];
+              swiglu_chunk(r, a_cur, b_cur, dav, dbv);
+              uint4* da_dst = reinterpret_cast<uint4*>(drow + h);
+              uint4* db_dst = reinterpret_cast<uint4*>(drow + p.H + h);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                da_dst[v] = dav[v];
+                db_dst[v] = dbv[v];
+              }
             }
-          }
-        }
-      } else if constexpr (MODE == kF2) {
-        const bool rv = row_local < t.cvalid;
-        const int64_t j = (int64_t)t.cm0 + row_local;
-        const bool whole = LRM_TC_FWD_STAGED && q * 32 + 32 <= t.cvalid;  // as in F1
-#pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c, r);
-          tmem_ld_wait();
-          const int col = t.n0 + c;
-          if (whole && col < p.D) {
-            uint4 yv[4];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              float f[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(r[8 * v + u]);
-              yv[v] = Vec16<__nv_bfloat16>::pack(f);
-            }
-            // one y block per warp: a second one in turn measured slower
-            uint8_t* yb = wst;
-            if (lane == 0) bulk_wait_read(0);
-            __syncwarp();
-            const int sw = (lane >> 1) & 3;
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              *reinterpret_cast<uint4*>(yb + lane * 64 + ((v ^ sw) << 4)) = yv[v];
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&maps.o1, yb, col, t.cm0 + q * 32);
-              bulk_commit();
-            }
-          } else if (rv && col < p.D) {
-            uint4* dst = reinterpret_cast<uint4*>(p.ob0 + j * p.D + col);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              float f[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(r[8 * v + u]);
-              dst[v] = Vec16<__nv_bfloat16>::pack(f);
+              a_cur[v] = a_nxt[v];
+              b_cur[v] = b_nxt[v];
             }
           }
-        }
-      } else {
-        const bool rows_in = WG ? (t.cm0 + q * 32 < row_lim) : (q * 32 < t.cvalid);
-        const bool whole = WG || (q * 32 + 32 <= t.cvalid);  // G4: block inside the group
+        } else if constexpr (MODE == kF1) {
+          // this warp's 64 gate columns and the matching 64 up columns
+          const bool rv = row_local < t.cvalid;
+          const int64_t j = (int64_t)t.cm0 + row_local;
+          const int hbase = ((warp - 2) >> 2) * (BN / 4);
+          // the warp's 32 rows inside the group (warp-uniform): a, b and phi go
+          // out as 32 x 32 blocks (64-byte swizzle) through TMA stores
+          const bool whole = LRM_TC_FWD_STAGED && q * 32 + 32 <= t.cvalid;
 #pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c, r);
-          tmem_ld_wait();
-          const int col = t.n0 + c;
-          if (!rows_in || col >= ncols) continue;
-          if (whole) {
-            staged_store(r, t, col);
-          } else if (row_local < t.cvalid) {  // G4 block crossing the group end
-            store_f32x32(p.out0 + (int64_t)(t.cm0 + row_local) * p.D + col, r);
+          for (int cc = 0; cc < BN / 4; cc += 32) {
+            const int hl = hbase + cc;
+            uint32_t ra[32], rb[32];
+            tmem_ld32(taddr + hl, ra);
+            tmem_ld32(taddr + BN / 2 + hl, rb);
+            tmem_ld_wait();
+            const int h = t.n0 / 2 + hl;
+            if (whole && h < p.H) {
+              uint4 av[4], bv[4], fv[4];
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float a[8], b[8], f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  a[u] = __uint_as_float(ra[8 * v + u]);
+                  b[u] = __uint_as_float(rb[8 * v + u]);
+                  f[u] = a[u] * __fdividef(1.0f, 1.0f + __expf(-a[u])) * b[u];
+                }
+                av[v] = Vec16<__nv_bfloat16>::pack(a);
+                bv[v] = Vec16<__nv_bfloat16>::pack(b);
+                fv[v] = Vec16<__nv_bfloat16>::pack(f);
+              }
+              // one set of blocks per warp: a second set costs a ring stage
+              // and measured slower
+              uint8_t* sb = wst;
+              if (lane == 0) bulk_wait_read(0);
+              __syncwarp();
+              const int sw = (lane >> 1) & 3;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                *reinterpret_cast<uint4*>(sb + lane * 64 + ((v ^ sw) << 4)) = av[v];
+                *reinterpret_cast<uint4*>(sb + 2048 + lane * 64 + ((v ^ sw) << 4)) = bv[v];
+                if (p.ob1)
+                  *reinterpret_cast<uint4*>(sb + 4096 + lane * 64 + ((v ^ sw) << 4)) = fv[v];
+              }
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&maps.o1, sb, h, t.cm0 + q * 32);
+                tma_store_2d(&maps.o1, sb + 2048, p.H + h, t.cm0 + q * 32);
+                if (p.ob1) tma_store_2d(&maps.o2, sb + 4096, h, t.cm0 + q * 32);
+                bulk_commit();
+              }
+            } else if (rv && h < p.H) {
+              __nv_bfloat16* arow = p.ob0 + j * 2 * p.H;
+              uint4* a_dst = reinterpret_cast<uint4*>(arow + h);
+              uint4* b_dst = reinterpret_cast<uint4*>(arow + p.H + h);
+              uint4* f_dst = p.ob1 ? reinterpret_cast<uint4*>(p.ob1 + j * p.H + h) : nullptr;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float a[8], b[8], f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  a[u] = __uint_as_float(ra[8 * v + u]);
+                  b[u] = __uint_as_float(rb[8 * v + u]);
+                  f[u] = a[u] * __fdividef(1.0f, 1.0f + __expf(-a[u])) * b[u];
+                }
+                a_dst[v] = Vec16<__nv_bfloat16>::pack(a);
+                b_dst[v] = Vec16<__nv_bfloat16>::pack(b);
+                if (f_dst) f_dst[v] = Vec16<__nv_bfloat16>::pack(f);
+              }
+            }
+          }
+        } else if constexpr (MODE == kF2) {
+          const bool rv = row_local < t.cvalid;
+          const int64_t j = (int64_t)t.cm0 + row_local;
+          const bool whole = LRM_TC_FWD_STAGED && q * 32 + 32 <= t.cvalid;  // as in F1
+#pragma unroll 1
+          for (int c = c_lo; c < c_hi; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c, r);
+            tmem_ld_wait();
+            const int col = t.n0 + c;
+            if (whole && col < p.D) {
+              uint4 yv[4];
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(r[8 * v + u]);
+                yv[v] = Vec16<__nv_bfloat16>::pack(f);
+              }
+              // one y block per warp: a second one in turn measured slower
+              uint8_t* yb = wst;
+              if (lane == 0) bulk_wait_read(0);
+              __syncwarp();
+              const int sw = (lane >> 1) & 3;
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                *reinterpret_cast<uint4*>(yb + lane * 64 + ((v ^ sw) << 4)) = yv[v];
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&maps.o1, yb, col, t.cm0 + q * 32);
+                bulk_commit();
+              }
+            } else if (rv && col < p.D) {
+              uint4* dst = reinterpret_cast<uint4*>(p.ob0 + j * p.D + col);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] = __uint_as_float(r[8 * v + u]);
+                dst[v] = Vec16<__nv_bfloat16>::pack(f);
+              }
+            }
+          }
+        } else {
+          const bool rows_in = WG ? (t.cm0 + q * 32 < row_lim) : (q * 32 < t.cvalid);
+          const bool whole = WG || (q * 32 + 32 <= t.cvalid);  // G4: block inside the group
+#pragma unroll 1
+          for (int c = c_lo; c < c_hi; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c, r);
+            tmem_ld_wait();
+            const int col = t.n0 + c;
+            if (!rows_in || col >= ncols) continue;
+            if (whole) {
+              staged_store(r, t, col);
+            } else if (row_local < t.cvalid) {  // G4 block crossing the group end
+              store_f32x32(p.out0 + (int64_t)(t.cm0 + row_local) * p.D + col, r);
+            }
           }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR && !leader) mbar_arrive_cluster(acc ? tempty_cl1 : tempty_cl0);
-        else mbar_arrive(&tempty[acc]);
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR && !leader) mbar_arrive_cluster(acc ? tempty_cl1 : tempty_cl0);
+          else mbar_arrive(&tempty[acc]);
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
       }
       if (quit) break;
     }
